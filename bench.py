@@ -1,0 +1,395 @@
+"""Benchmark of the Q4 verify matmul on GB300.
+
+Default workload: the attention input projection of the 27B-class hybrid
+(K = 5120 -> N = 14336, Q4 group-64 weights), verify rows swept M = 1, 2, 4, 8,
+16.  One step = for each M, `reps` calls of q4_matmul, each on a different copy
+of the weights from a rotating pool larger than L2, captured once into a CUDA
+graph and replayed.  value = algorithmic HBM bytes of the step / device time,
+bytes per call = N*K*0.5625 + M*K*2 + M*N*4 (weights once, x once, y once).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload attn_sweep|lm_head|mlp_gdn]
+
+Under torchrun each rank runs its own replica (the path needs no exchange);
+rank 0 prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Q4 verify-matmul HBM GB/s (% of GB300 peak) at M=1..16; M=16/M=1 time ratio"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["attn_sweep", "lm_head", "mlp_gdn"], default="attn_sweep")
+    p.add_argument("--reps", type=int, default=20, help="calls per M per step")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload_spec(name):
+    """List of (label, N, K, [M...]) and the workload's description."""
+    import synth_inputs as si
+    if name == "attn_sweep":
+        N, K = si.SHAPES["attn_in"]
+        return [("attn_in", N, K, [1, 2, 4, 8, 16])], "attention input projection K=5120->N=14336, M sweep 1,2,4,8,16"
+    if name == "lm_head":
+        N, K = si.SHAPES["lm_head"]
+        return [("lm_head", N, K, [16, 16])], "LM head K=5120->N=248320, M=16, twice per step"
+    shapes = [(n, *si.SHAPES[n], [1, 16]) for n in ("gate_up", "down", "gdn_in", "gdn_out")]
+    return shapes, "MLP + GDN projections (gate/up, down, GDN in, GDN out), M=1 and 16"
+
+
+def call_bytes(M, N, K):
+    return N * K * 9 // 16 + M * K * 2 + M * N * 4
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_row_speculative_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as fh:
+            h.update(fn.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, only if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.out = None
+        try:
+            self.out = open(os.devnull if gpu_id is None else os.path.join("/tmp", f"q4clk_{os.getpid()}.csv"), "w+")
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if gpu_id:
+                cmd += ["-i", gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 7]
+        try:
+            os.unlink(self.out.name)
+        except OSError:
+            pass
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
+        power = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def cpu_oracle_sample(spec, seconds, seed=0):
+    """Time the CPU oracle on a bounded sample of the workload: every M of the
+    sweep over a subset of output columns; GB/s with the same byte formula."""
+    import numpy as np
+    import oracle
+    import synth_inputs as si
+    oracle.build()
+    label, N, K, Ms = spec[0]
+    W = si.make_weights(N, K, 424242).numpy()
+    threads = os.cpu_count() or 1
+    xs = {M: si.bf16_bits(si.make_x(M, K, 99 + M)).numpy().view(np.uint16) for M in set(Ms)}
+    # calibrate the column count on a small probe
+    probe = 64
+    t0 = time.perf_counter()
+    for M in Ms:
+        oracle.matmul(xs[M], W, N, K, cols=np.arange(probe), threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    ncols = int(min(N, max(probe, probe * seconds / dt)))
+    cols = np.arange(ncols)
+    t0 = time.perf_counter()
+    for M in Ms:
+        oracle.matmul(xs[M], W, N, K, cols=cols, threads=threads)
+    el = time.perf_counter() - t0
+    nbytes = sum(call_bytes(M, ncols, K) for M in Ms)
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{label} K={K}, first {ncols} of {N} output columns, M in {Ms}, fp64 oracle, "
+                      f"{el:.1f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    spec, desc = workload_spec(args.workload)
+    per_step = []
+    cb = None
+    for _ in range(args.warmup + args.steps):
+        cb = cpu_oracle_sample(spec, max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))))
+        per_step.append(cb["value"])
+    vals = per_step[args.warmup:]
+    value = statistics.mean(vals)
+    label, N, K, Ms = spec[0]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "N": N, "K": K, "M": Ms},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": value,
+                             "unit": "GB/s"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import bit_row_speculative_gb300 as q4
+    import synth_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    spec, desc = workload_spec(args.workload)
+
+    # prediction first: the byte count and the ceiling at the measured peak
+    peak, peak_kind = read_peaks()
+    step_bytes = sum(call_bytes(M, N, K) for _, N, K, Ms in spec for M in Ms) * args.reps
+    if rank == 0:
+        print(f"prediction: {step_bytes / 1e9:.3f} GB per step at {peak:.0f} GB/s ({peak_kind}) "
+              f"-> {step_bytes / peak / 1e6:.3f} ms per step floor", file=sys.stderr, flush=True)
+
+    # rotating pools of distinct weight copies, each pool > 4x L2
+    pools = {}
+    for label, N, K, Ms in spec:
+        nbytes = N * K * 9 // 16
+        copies = max(2, -(-4 * l2 // nbytes))
+        base = si.make_weights(N, K, si.w_seed(2, 0) + 7 * rank, device=dev)
+        pools[label] = [base] + [base.clone() for _ in range(copies - 1)]
+    xs = {(label, M): si.make_x(M, K, si.x_seed(2) + M, device=dev) for label, N, K, Ms in spec for M in Ms}
+    ys = {(label, M): torch.empty((M, N), dtype=torch.float32, device=dev) for label, N, K, Ms in spec for M in Ms}
+
+    stream = torch.cuda.Stream(device=dev)
+    launches_per_call = 1
+
+    def enqueue(label, N, K, M, i):
+        W = pools[label][i % len(pools[label])]
+        q4.matmul(xs[(label, M)], W, N, K, y=ys[(label, M)])
+
+    # warm-up (eager), then one CUDA graph per (shape, M) holding `reps` calls
+    counter = 0
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for label, N, K, Ms in spec:
+                for M in Ms:
+                    for r in range(args.reps):
+                        enqueue(label, N, K, M, counter)
+                        counter += 1
+    stream.synchronize()
+    q4.device_status(stream)
+
+    graphs = []
+    for label, N, K, Ms in spec:
+        for M in Ms:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(args.reps):
+                    enqueue(label, N, K, M, counter)
+                    counter += 1
+            graphs.append((label, N, K, M, g))
+    with torch.cuda.stream(stream):
+        for *_, g in graphs:          # one untimed replay of each graph
+            g.replay()
+    stream.synchronize()
+
+    per_graph_ms = {i: 0.0 for i in range(len(graphs))}
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in graphs]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            for i, (label, N, K, M, g) in enumerate(graphs):
+                evs[i][0].record(stream)
+                g.replay()
+                evs[i][1].record(stream)
+            # accumulate per-graph times after each step (events are reused)
+            stream.synchronize()
+            for i in range(len(graphs)):
+                per_graph_ms[i] += evs[i][0].elapsed_time(evs[i][1])
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    q4.device_status(stream)
+    if world > 1:
+        torch.distributed.barrier()
+
+    kernel_ms = sum(per_graph_ms.values())            # device time of the matmul calls only
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([kernel_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        kernel_ms = float(t.item())
+    value = world * step_bytes * args.steps / (kernel_ms / 1e3) / 1e9
+
+    per_m = {}
+    for i, (label, N, K, M, g) in enumerate(graphs):
+        us = per_graph_ms[i] / (args.steps * args.reps) * 1e3
+        per_m[f"{label}_M{M}"] = {"us_per_call": round(us, 3),
+                                  "GBs": round(call_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
+    ratio = None
+    if args.workload == "attn_sweep":
+        ratio = per_m["attn_in_M16"]["us_per_call"] / per_m["attn_in_M1"]["us_per_call"]
+
+    # end to end through the public API with host buffers: per call, pinned
+    # host x -> device, the matmul, device y -> pinned host
+    e2e = None
+    if True:
+        hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
+        hy = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in ys.items()}
+        dx = {k: torch.empty_like(v) for k, v in xs.items()}
+        h2d = sum(hx[(label, M)].numel() * 2 for label, N, K, Ms in spec for M in Ms) * args.reps
+        d2h = sum(hy[(label, M)].numel() * 4 for label, N, K, Ms in spec for M in Ms) * args.reps
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e_steps = max(1, min(args.steps, 5))
+        with torch.cuda.stream(stream):
+            for s in range(e_steps + 1):
+                if s == 1:
+                    e0.record(stream)
+                for label, N, K, Ms in spec:
+                    for M in Ms:
+                        for r in range(args.reps):
+                            dx[(label, M)].copy_(hx[(label, M)], non_blocking=True)
+                            W = pools[label][(r * 5 + M) % len(pools[label])]
+                            q4.matmul(dx[(label, M)], W, N, K, y=ys[(label, M)])
+                            hy[(label, M)].copy_(ys[(label, M)], non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        e_ms = e0.elapsed_time(e1) / e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * step_bytes / (e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+
+    if rank != 0:
+        return
+    n_calls = sum(len(Ms) for _, _, _, Ms in spec) * args.reps
+    achieved = step_bytes / (kernel_ms / args.steps / 1e3) / 1e9
+    traffic = read_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(kernel_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x, q4 weights, fp32 accumulate",
+        "data": "synthetic (seeded; nibbles uniform 0..15, scale |N(0,1)|*0.01, bias -8*scale+N(0,1e-3), x N(0,1))",
+        "config": {"workload": desc, "calls_per_M_per_step": args.reps,
+                   "l2": f"rotating pool of {len(next(iter(pools.values())))} weight copies "
+                         f"({sum(w.numel() for w in next(iter(pools.values()))) / 1e6:.0f} MB) > L2 "
+                         f"({l2 / 2**20:.0f} MiB); one CUDA graph per M",
+                   "parallelism": f"replicas x{world}"},
+        "per_M": per_m, "ratio_M16_over_M1": None if ratio is None else round(ratio, 4),
+        "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": step_bytes // n_calls},
+        "gpu_launches": n_calls * launches_per_call * args.steps,
+        "clocks": clocks, "e2e": e2e, "timed_region_ms": round(total_ms, 3),
+    }
+    if not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_oracle_sample(spec, args.cpu_seconds)
+        except Exception as exc:                     # report, do not hide
+            line["cpu_baseline"] = {"error": repr(exc)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

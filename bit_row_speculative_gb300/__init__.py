@@ -1,0 +1,121 @@
+"""Python binding of libq4 (include/q4.h): argument marshalling only.
+
+Every step of the verify matmul runs in the library's CUDA kernels; PyTorch
+only supplies device memory and streams.  The binding fails loudly when the
+compiled library is missing -- there is no fallback path.
+
+Build the library with ``python -c "import __graft_entry__ as g; g.build()"``
+(or ``python bit_row_speculative_gb300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libq4.so")
+
+Q4_OK = 0
+Q4_ERR_INVALID_ARG = 1
+Q4_ERR_UNSUPPORTED_SHAPE = 2
+Q4_ERR_MISALIGNED = 3
+Q4_ERR_UNSUPPORTED_DEVICE = 4
+Q4_ERR_CUDA = 5
+Q4_ERR_TIMEOUT = 6
+Q4_ERR_OVERFLOW = 7
+MAX_ROWS = 16
+GROUP = 64
+
+# Exported symbols (one per function declared in include/q4.h).
+SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_device_status", "q4_last_error", "q4_status_string")
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_name(status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib: ctypes.CDLL) -> None:
+    c = ctypes
+    lib.q4_packed_bytes.restype = c.c_uint64
+    lib.q4_packed_bytes.argtypes = [c.c_uint64, c.c_uint64]
+    lib.q4_matmul.restype = c.c_int
+    lib.q4_matmul.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p]
+    lib.q4_device_status.restype = c.c_int
+    lib.q4_device_status.argtypes = [c.c_void_p]
+    lib.q4_last_error.restype = c.c_char_p
+    lib.q4_last_error.argtypes = []
+    lib.q4_status_string.restype = c.c_char_p
+    lib.q4_status_string.argtypes = [c.c_int]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libq4.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libq4.so is not built ({LIB_PATH} missing); run __graft_entry__.build()")
+            handle = ctypes.CDLL(LIB_PATH)
+            _declare(handle)
+            _lib = handle
+        return _lib
+
+
+def status_name(status: int) -> str:
+    try:
+        return lib().q4_status_string(status).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _check(status: int) -> None:
+    if status != Q4_OK:
+        raise Q4Error(status, lib().q4_last_error().decode())
+
+
+def packed_bytes(N: int, K: int) -> int:
+    return int(lib().q4_packed_bytes(N, K))
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def matmul(x, W, N: int, K: int, y=None, stream=None):
+    """y[M, N] (fp32) = x[M, K] (bf16) times the packed Q4 matrix W[N, K]."""
+    import torch
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bfloat16 tensor")
+    if W.dtype != torch.uint8 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous uint8 tensor")
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError(f"x has {x.shape[1]} columns, K = {K}")
+    if W.numel() != packed_bytes(N, K):
+        raise ValueError(f"W has {W.numel()} bytes, expected {packed_bytes(N, K)}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    elif y.dtype != torch.float32 or tuple(y.shape) != (M, N) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float32 [M, N] tensor")
+    _check(lib().q4_matmul(x.data_ptr(), W.data_ptr(), M, N, K, y.data_ptr(), _stream_handle(stream)))
+    return y
+
+
+def matmul_raw(x_ptr: int, W_ptr: int, M: int, N: int, K: int, y_ptr: int, stream_handle: int) -> None:
+    """Pointer-level call of q4_matmul (for callers that manage their own buffers)."""
+    _check(lib().q4_matmul(x_ptr, W_ptr, M, N, K, y_ptr, stream_handle))
+
+
+def device_status(stream=None) -> None:
+    """Synchronise and raise Q4Error(Q4_ERR_TIMEOUT) if a device-side wait gave up."""
+    _check(lib().q4_device_status(_stream_handle(stream)))

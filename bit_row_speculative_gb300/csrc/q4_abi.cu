@@ -1,0 +1,185 @@
+// Host side of the C ABI declared in include/q4.h: argument checks, the launch
+// plan (chosen from N, K and the device's SM count only, never from M) and the
+// kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "q4.h"
+#include "q4_generic.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+q4_status fail(q4_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+q4_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(Q4_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    q4_status status = Q4_OK;
+    std::string error;
+    int sm_count = 0;
+};
+
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+template <int MT>
+cudaError_t prepare_generic() {
+    return cudaFuncSetAttribute(q4::generic::matmul_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)q4::generic::smem_bytes(MT));
+}
+
+// One-time per-device set-up: capability check and kernel attributes.
+q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(Q4_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        if (prop.major != 10 || prop.minor != 3) {
+            d.status = Q4_ERR_UNSUPPORTED_DEVICE;
+            char buf[512];
+            snprintf(buf, sizeof buf, "device %d (%s) is compute %d.%d; this library is built for 10.3 (sm_103a)",
+                     dev, prop.name, prop.major, prop.minor);
+            d.error = buf;
+        } else {
+            d.sm_count = prop.multiProcessorCount;
+            cudaError_t a = prepare_generic<1>();
+            if (a == cudaSuccess) a = prepare_generic<2>();
+            if (a == cudaSuccess) a = prepare_generic<4>();
+            if (a == cudaSuccess) a = prepare_generic<8>();
+            if (a == cudaSuccess) a = prepare_generic<16>();
+            if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
+            d.status = Q4_OK;
+        }
+        d.ready = true;
+    }
+    if (d.status != Q4_OK) return fail(d.status, "%s", d.error.c_str());
+    *dev_out = dev;
+    *info_out = &d;
+    return Q4_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int rows_template(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
+q4_status launch_generic(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                         cudaStream_t stream) {
+    using namespace q4::generic;
+    const int64_t blocks = (N + kRowsPerCta - 1) / kRowsPerCta;
+    if (blocks > 0x7FFFFFFF) return fail(Q4_ERR_INVALID_ARG, "N = %lld needs too many blocks", (long long)N);
+    const int MT = rows_template(M);
+    const dim3 grid((unsigned)blocks), block(kWarps * 32);
+    const size_t smem = smem_bytes(MT);
+    auto xp = static_cast<const uint16_t*>(x);
+    auto wp = static_cast<const uint8_t*>(W);
+    switch (MT) {
+        case 1: matmul_kernel<1><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+        case 2: matmul_kernel<2><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+        case 4: matmul_kernel<4><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+        case 8: matmul_kernel<8><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+        default: matmul_kernel<16><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launching the generic Q4 kernel");
+    return Q4_OK;
+}
+
+}  // namespace
+
+// Set by a kernel whose bounded device-side wait ran out (never by a trap).
+__device__ unsigned int q4_device_error_word = 0;
+
+extern "C" {
+
+uint64_t q4_packed_bytes(uint64_t N, uint64_t K) {
+    if (N == 0 || K == 0 || (K % 64) != 0) return 0;
+    if (K > UINT64_MAX / N) return 0;
+    const uint64_t per16 = (N * K) / 16;
+    if (per16 > UINT64_MAX / 9) return 0;
+    return per16 * 9;
+}
+
+q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                    q4_stream_t stream) {
+    g_last_error.clear();
+    if (!x || !W || !y) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (x=%p W=%p y=%p)", x, W, (void*)y);
+    if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
+    if (N < 1) return fail(Q4_ERR_INVALID_ARG, "N = %lld must be >= 1", (long long)N);
+    if (K < 64 || (K % 64) != 0)
+        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "K = %lld must be a positive multiple of 64", (long long)K);
+    if (q4_packed_bytes((uint64_t)N, (uint64_t)K) == 0)
+        return fail(Q4_ERR_OVERFLOW, "packed size of %lld x %lld overflows", (long long)N, (long long)K);
+    if ((uint64_t)M * (uint64_t)N > (1ull << 40))
+        return fail(Q4_ERR_INVALID_ARG, "output of %d x %lld is too large", M, (long long)N);
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y))
+        return fail(Q4_ERR_MISALIGNED, "x, W and y must be 16-byte aligned (x=%p W=%p y=%p)", x, W, (void*)y);
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    q4_status s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    return launch_generic(x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status q4_device_status(q4_stream_t stream) {
+    g_last_error.clear();
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    q4_status s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, q4_device_error_word, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(q4_device_error_word, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        return fail(Q4_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    }
+    return Q4_OK;
+}
+
+const char* q4_last_error(void) { return g_last_error.c_str(); }
+
+const char* q4_status_string(q4_status s) {
+    switch (s) {
+        case Q4_OK: return "Q4_OK";
+        case Q4_ERR_INVALID_ARG: return "Q4_ERR_INVALID_ARG";
+        case Q4_ERR_UNSUPPORTED_SHAPE: return "Q4_ERR_UNSUPPORTED_SHAPE";
+        case Q4_ERR_MISALIGNED: return "Q4_ERR_MISALIGNED";
+        case Q4_ERR_UNSUPPORTED_DEVICE: return "Q4_ERR_UNSUPPORTED_DEVICE";
+        case Q4_ERR_CUDA: return "Q4_ERR_CUDA";
+        case Q4_ERR_TIMEOUT: return "Q4_ERR_TIMEOUT";
+        case Q4_ERR_OVERFLOW: return "Q4_ERR_OVERFLOW";
+    }
+    return "Q4_ERR_UNKNOWN";
+}
+
+}  // extern "C"

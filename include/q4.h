@@ -1,0 +1,93 @@
+/*
+ * q4.h -- C ABI of the GB300 Q4 verify-matmul library (libq4.so).
+ *
+ * The operation.  A speculative-decoding verify pass multiplies M = 1..16 draft
+ * or tree rows against every quantized weight of a layer, reading the weights
+ * from HBM once ("Faster, with the same words" (goinfer.dev), section "The
+ * problem": a step that checks eight tokens costs much less than eight steps,
+ * because the weights are read once; "qwen-spec" (jonasloos.github.io), Notes:
+ * a 4-bit matmul that reads every weight tile once and multiplies all rows at
+ * once).  For x[M,K] (bf16) and a packed Q4 matrix W[N,K]:
+ *
+ *     y[m,n] = sum_k x[m,k] * ( s[n,k/64] * q[n,k] + b[n,k/64] )
+ *
+ * Packed format ("Splash engine" analysis (ai.thesatyajit.com), section "The
+ * engine hard-codes the model": nine bytes per sixteen weights -- 32 bytes of
+ * unsigned nibbles plus a bf16 scale and a bf16 bias per group of 64 inputs).
+ * Byte layout fixed by this library (planar, row-major), N*K/16*9 bytes:
+ *     [nibbles: N rows x K/2 bytes; byte j of a row holds input 2j in bits 0-3
+ *               and input 2j+1 in bits 4-7]
+ *     [scales:  N rows x K/64 bf16, little-endian]
+ *     [biases:  N rows x K/64 bf16, little-endian]
+ *
+ * Conventions for every call below:
+ *   - All buffers are owned by the caller.  Device pointers must be device
+ *     memory of the current CUDA device (or managed memory).
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are detected on the host and returned before anything
+ *     is launched; launch failures return Q4_ERR_CUDA.  A device-side wait
+ *     that ran out of time is reported by q4_device_status().
+ *   - On any status other than Q4_OK, q4_last_error() describes the failure
+ *     (a thread-local string, valid until the next call on that thread).
+ *   - Results are deterministic, and row m of y does not depend on M or on
+ *     the contents of the other rows of x (bit-identical batched verify:
+ *     "Faster, with the same words", section "How it works").
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* q4_stream_t;
+
+typedef enum {
+    Q4_OK = 0,
+    Q4_ERR_INVALID_ARG = 1,        /* null pointer, M out of 1..16, N < 1, ...     */
+    Q4_ERR_UNSUPPORTED_SHAPE = 2,  /* K not a positive multiple of 64              */
+    Q4_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned             */
+    Q4_ERR_UNSUPPORTED_DEVICE = 4, /* the current device is not compute 10.3       */
+    Q4_ERR_CUDA = 5,               /* a CUDA runtime call failed                   */
+    Q4_ERR_TIMEOUT = 6,            /* a device-side wait gave up (q4_device_status) */
+    Q4_ERR_OVERFLOW = 7            /* a byte count does not fit in 64 bits          */
+} q4_status;
+
+#define Q4_MAX_ROWS 16
+
+/* Bytes of a packed N x K matrix: the page's q4PackedBytes -- an
+ * overflow-checked (N*K/16)*9 ("Splash engine", section "The engine hard-codes
+ * the model").  Returns 0 when N == 0, K is not a positive multiple of 64, or
+ * the product overflows 64 bits.  Host only; never touches the GPU. */
+uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
+
+/* y[M,N] = x[M,K] * W[N,K]^T with W dequantized as above.
+ *   x : device, bf16, row-major [M, K], 16-byte aligned.
+ *   W : device, packed buffer of exactly q4_packed_bytes(N, K) bytes, 16-byte aligned.
+ *   M : 1..16 verify rows.   N : >= 1 outputs.   K : positive multiple of 64.
+ *   y : device, fp32, row-major [M, N], 16-byte aligned; fully overwritten.
+ * Allocates no device memory.
+ * Accuracy: |y - exact| <= 2e-3 * sum_k |x[m,k] w[n,k]| per output. */
+q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                    q4_stream_t stream);
+
+/* Synchronizes `stream` and reports whether any kernel of this library on the
+ * current device gave up a bounded device-side wait since the last query
+ * (Q4_ERR_TIMEOUT), then clears that record.  Q4_OK otherwise. */
+q4_status q4_device_status(q4_stream_t stream);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* q4_last_error(void);
+
+/* Constant name of a status code. */
+const char* q4_status_string(q4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4_H */

@@ -1,0 +1,66 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/q4.h declares, computes the packed size exactly like the
+oracle's closed form, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_row_speculative_gb300 as q4
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(q4_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol():
+    lib = q4.lib()
+    declared = declared_functions()
+    assert "q4_matmul" in declared and "q4_packed_bytes" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(q4.SYMBOLS)
+
+
+@pytest.mark.parametrize("N,K", [(256, 512), (14336, 5120), (34816, 5120), (5120, 17408), (16640, 5120),
+                                 (5120, 6144), (248320, 5120), (1, 64), (7, 192), (0, 64), (3, 100),
+                                 (1, 0), (1 << 40, 1 << 40), ((1 << 58) + 1, 64)])
+def test_packed_bytes_matches_oracle(N, K):
+    assert q4.packed_bytes(N, K) == oracle.packed_bytes(N, K)
+
+
+def test_status_strings():
+    for code, name in [(0, "Q4_OK"), (1, "Q4_ERR_INVALID_ARG"), (6, "Q4_ERR_TIMEOUT"), (7, "Q4_ERR_OVERFLOW")]:
+        assert q4.status_name(code) == name
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 16, 1, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),        # null x
+    ((16, 0, 1, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),        # null W
+    ((16, 16, 1, 256, 512, 0), q4.Q4_ERR_INVALID_ARG),        # null y
+    ((16, 16, 0, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),       # M = 0
+    ((16, 16, 17, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),      # M = 17
+    ((16, 16, 1, 0, 512, 16), q4.Q4_ERR_INVALID_ARG),         # N = 0
+    ((16, 16, 1, 256, 96, 16), q4.Q4_ERR_UNSUPPORTED_SHAPE),  # K % 64 != 0
+    ((16, 16, 1, 256, 0, 16), q4.Q4_ERR_UNSUPPORTED_SHAPE),   # K = 0
+    ((16, 16, 1, 1 << 40, 1 << 40, 16), q4.Q4_ERR_OVERFLOW),  # packed size overflows
+    ((8, 16, 1, 256, 512, 16), q4.Q4_ERR_MISALIGNED),         # x misaligned
+    ((16, 24, 1, 256, 512, 16), q4.Q4_ERR_MISALIGNED),        # W misaligned
+])
+def test_argument_errors_return_before_launch(args, status):
+    lib = q4.lib()
+    rc = lib.q4_matmul(*args, None)
+    assert rc == status, (rc, lib.q4_last_error())
+    assert lib.q4_last_error().decode() != ""
