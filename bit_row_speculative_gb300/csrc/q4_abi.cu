@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/q4.h: argument checks, the launch
 // plan (chosen from N, K and the device's SM count only, never from M) and the
 // kernel launches on the caller's stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -11,6 +12,10 @@
 
 #include "q4.h"
 #include "q4_generic.cuh"
+#include "q4_tc.cuh"
+
+// Set by a kernel whose bounded device-side wait ran out (never by a trap).
+__device__ unsigned int q4_device_error_word = 0;
 
 namespace {
 
@@ -37,10 +42,24 @@ struct DeviceInfo {
     q4_status status = Q4_OK;
     std::string error;
     int sm_count = 0;
+    float* partials = nullptr;      // split-K partial sums of the tensor-core kernel
+    int* sems = nullptr;            // per-tile arrival counters (zero between launches)
+    unsigned int* error_word = nullptr;
 };
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
 
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mutex;
+
+template <int MT>
+cudaError_t prepare_tc() {
+    return cudaFuncSetAttribute(q4::tc::q4_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                q4::tc::smem_bytes());
+}
 
 template <int MT>
 cudaError_t prepare_generic() {
@@ -73,7 +92,29 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_generic<4>();
             if (a == cudaSuccess) a = prepare_generic<8>();
             if (a == cudaSuccess) a = prepare_generic<16>();
+            if (a == cudaSuccess) a = prepare_tc<1>();
+            if (a == cudaSuccess) a = prepare_tc<2>();
+            if (a == cudaSuccess) a = prepare_tc<4>();
+            if (a == cudaSuccess) a = prepare_tc<8>();
+            if (a == cudaSuccess) a = prepare_tc<16>();
             if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
+            if (!g_encode) {
+                void* fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                a = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+                if (a != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                    return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+            }
+            // scratch of the tensor-core kernel, sized for one CTA per SM
+            const size_t pbytes = q4::tc::partial_floats(d.sm_count) * sizeof(float);
+            const size_t sbytes = q4::tc::sem_ints(d.sm_count) * sizeof(int);
+            a = cudaMalloc(&d.partials, pbytes);
+            if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
+            if (a == cudaSuccess) a = cudaMemset(d.sems, 0, sbytes);
+            if (a == cudaSuccess) a = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), q4_device_error_word);
+            if (a == cudaSuccess) a = cudaDeviceSynchronize();
+            if (a != cudaSuccess) return cuda_fail(a, "allocating the library scratch");
             d.status = Q4_OK;
         }
         d.ready = true;
@@ -110,10 +151,63 @@ q4_status launch_generic(const void* x, const void* W, int M, int64_t N, int64_t
     return Q4_OK;
 }
 
-}  // namespace
+q4_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return Q4_OK;
+}
 
-// Set by a kernel whose bounded device-side wait ran out (never by a trap).
-__device__ unsigned int q4_device_error_word = 0;
+q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                    cudaStream_t stream) {
+    using namespace q4::tc;
+    CUtensorMap map_nib, map_x;
+    q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
+                            (uint64_t)K / 2, 32, kRowsCG, CU_TENSOR_MAP_SWIZZLE_32B);
+    if (s != Q4_OK) return s;
+    s = encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, 16,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (s != Q4_OK) return s;
+    Params p;
+    p.W = static_cast<const uint8_t*>(W);
+    p.y = y;
+    p.partials = d.partials;
+    p.sems = d.sems;
+    p.error_word = d.error_word;
+    p.N = N;
+    p.K = K;
+    p.M = M;
+    p.G = (int)(K / 64);
+    p.T = (int)((N + kRowsTile - 1) / kRowsTile);
+    p.U = (int64_t)p.T * p.G;
+    p.C = (int)(p.U < d.sm_count ? p.U : d.sm_count);
+    const dim3 grid((unsigned)p.C), block(kThreads);
+    const size_t smem = (size_t)smem_bytes();
+    switch (rows_template(M)) {
+        case 1: q4_tc_kernel<1><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
+        case 2: q4_tc_kernel<2><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
+        case 4: q4_tc_kernel<4><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
+        case 8: q4_tc_kernel<8><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
+        default: q4_tc_kernel<16><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launching the tensor-core Q4 kernel");
+    return Q4_OK;
+}
+
+// The launch plan depends on N, K and the device only -- never on M -- so a
+// row's result is the same for every M.
+bool use_tc(int64_t N, int64_t K) {
+    return (K % 512) == 0 && (N / q4::tc::kRowsTile) < (int64_t)1 << 30;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -143,6 +237,7 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
     const DeviceInfo* info = nullptr;
     q4_status s = device_setup(&dev, &info);
     if (s != Q4_OK) return s;
+    if (use_tc(N, K)) return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
     return launch_generic(x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
