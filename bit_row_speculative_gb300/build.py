@@ -37,18 +37,18 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, out: str = LIB) -> str:
+    if not force and out == LIB and up_to_date():
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I", INCLUDE, "-I", CSRC, "-o", LIB + ".tmp",
+           "-I", INCLUDE, "-I", CSRC, "-o", out + ".tmp",
            *[os.path.join(CSRC, s) for s in SOURCES], *(extra or [])]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.run(cmd, check=True)
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+    os.replace(out + ".tmp", out)
+    return out
 
 
 if __name__ == "__main__":

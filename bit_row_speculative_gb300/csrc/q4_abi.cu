@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "q4.h"
 #include "q4_generic.cuh"
@@ -44,6 +45,7 @@ struct DeviceInfo {
     int sm_count = 0;
     float* partials = nullptr;      // split-K partial sums of the tensor-core kernel
     int* sems = nullptr;            // per-tile arrival counters (zero between launches)
+    uint8_t* xt = nullptr;          // prepared x records (one per group of 64 inputs)
     unsigned int* error_word = nullptr;
 };
 
@@ -51,6 +53,13 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+#ifdef Q4_TRACE
+unsigned long long* g_trace = nullptr;
+#endif
+
+// The tensor-core path serves K up to 64 * kTcMaxGroups (the prepared-x scratch).
+constexpr int64_t kTcMaxGroups = 2048;
 
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mutex;
@@ -111,6 +120,7 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             const size_t sbytes = q4::tc::sem_ints(d.sm_count) * sizeof(int);
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
+            if (a == cudaSuccess) a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * q4::prep::kRecordBytes);
             if (a == cudaSuccess) a = cudaMemset(d.sems, 0, sbytes);
             if (a == cudaSuccess) a = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), q4_device_error_word);
             if (a == cudaSuccess) a = cudaDeviceSynchronize();
@@ -164,18 +174,35 @@ q4_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
     return Q4_OK;
 }
 
+// Launch `kernel` on `stream` with programmatic stream serialization, so that
+// it may start while the preceding kernel finishes (it waits on the device
+// with griddepcontrol.wait before touching that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     cudaStream_t stream) {
     using namespace q4::tc;
-    CUtensorMap map_nib, map_x;
+    CUtensorMap map_nib;
     q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
-                            (uint64_t)K / 2, 32, kRowsCG, CU_TENSOR_MAP_SWIZZLE_32B);
-    if (s != Q4_OK) return s;
-    s = encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, 16,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+                            (uint64_t)K / 2, 64, kRowsCG, CU_TENSOR_MAP_SWIZZLE_64B);
     if (s != Q4_OK) return s;
     Params p;
     p.W = static_cast<const uint8_t*>(W);
+    p.xt = d.xt;
     p.y = y;
     p.partials = d.partials;
     p.sems = d.sems;
@@ -185,18 +212,23 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
     p.M = M;
     p.G = (int)(K / 64);
     p.T = (int)((N + kRowsTile - 1) / kRowsTile);
-    p.U = (int64_t)p.T * p.G;
-    p.C = (int)(p.U < d.sm_count ? p.U : d.sm_count);
+    p.U = p.T * p.G;
+    p.C = p.U < d.sm_count ? p.U : d.sm_count;
+#ifdef Q4_TRACE
+    p.trace = g_trace;
+#endif
+    cudaError_t e = launch_pdl(q4::prep::prep_x_kernel, dim3((unsigned)p.G), dim3(q4::prep::kThreads), 0, stream,
+                               static_cast<const uint16_t*>(x), M, K, d.xt);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the x preparation kernel");
     const dim3 grid((unsigned)p.C), block(kThreads);
     const size_t smem = (size_t)smem_bytes();
     switch (rows_template(M)) {
-        case 1: q4_tc_kernel<1><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
-        case 2: q4_tc_kernel<2><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
-        case 4: q4_tc_kernel<4><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
-        case 8: q4_tc_kernel<8><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
-        default: q4_tc_kernel<16><<<grid, block, smem, stream>>>(map_nib, map_x, p); break;
+        case 1: e = launch_pdl(q4_tc_kernel<1>, grid, block, smem, stream, map_nib, p); break;
+        case 2: e = launch_pdl(q4_tc_kernel<2>, grid, block, smem, stream, map_nib, p); break;
+        case 4: e = launch_pdl(q4_tc_kernel<4>, grid, block, smem, stream, map_nib, p); break;
+        case 8: e = launch_pdl(q4_tc_kernel<8>, grid, block, smem, stream, map_nib, p); break;
+        default: e = launch_pdl(q4_tc_kernel<16>, grid, block, smem, stream, map_nib, p); break;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launching the tensor-core Q4 kernel");
     return Q4_OK;
 }
@@ -204,7 +236,9 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
 // The launch plan depends on N, K and the device only -- never on M -- so a
 // row's result is the same for every M.
 bool use_tc(int64_t N, int64_t K) {
-    return (K % 512) == 0 && (N / q4::tc::kRowsTile) < (int64_t)1 << 30;
+    // the kernel's schedule arithmetic is 32-bit: tiles x groups must fit
+    return (K % 512) == 0 && K / 64 <= kTcMaxGroups &&
+           ((N + q4::tc::kRowsTile - 1) / q4::tc::kRowsTile) * (K / 64) < ((int64_t)1 << 30);
 }
 
 }  // namespace
@@ -262,6 +296,11 @@ q4_status q4_device_status(q4_stream_t stream) {
 }
 
 const char* q4_last_error(void) { return g_last_error.c_str(); }
+
+#ifdef Q4_TRACE
+// Developer timing trace (only in builds made with -DQ4_TRACE).
+void q4_debug_set_trace(void* device_buffer) { g_trace = static_cast<unsigned long long*>(device_buffer); }
+#endif
 
 const char* q4_status_string(q4_status s) {
     switch (s) {
