@@ -9,11 +9,14 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <algorithm>
+#include <cstdlib>
 #include <utility>
 
 #include "q4.h"
 #include "q4_generic.cuh"
 #include "q4_tc.cuh"
+#include "q4_mma.cuh"
 
 // Set by a kernel whose bounded device-side wait ran out (never by a trap).
 __device__ unsigned int q4_device_error_word = 0;
@@ -64,6 +67,12 @@ constexpr int64_t kTcMaxGroups = 2048;
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mutex;
 
+template <int NT>
+cudaError_t prepare_rk() {
+    return cudaFuncSetAttribute(q4::rk::q4_rk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                q4::rk::smem_bytes());
+}
+
 template <int MT>
 cudaError_t prepare_tc() {
     return cudaFuncSetAttribute(q4::tc::q4_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -106,6 +115,8 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_tc<4>();
             if (a == cudaSuccess) a = prepare_tc<8>();
             if (a == cudaSuccess) a = prepare_tc<16>();
+            if (a == cudaSuccess) a = prepare_rk<1>();
+            if (a == cudaSuccess) a = prepare_rk<2>();
             if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
             if (!g_encode) {
                 void* fn = nullptr;
@@ -116,8 +127,9 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
                 g_encode = reinterpret_cast<EncodeTiledFn>(fn);
             }
             // scratch of the tensor-core kernel, sized for one CTA per SM
-            const size_t pbytes = q4::tc::partial_floats(d.sm_count) * sizeof(float);
-            const size_t sbytes = q4::tc::sem_ints(d.sm_count) * sizeof(int);
+            const size_t pbytes = std::max(q4::tc::partial_floats(d.sm_count), q4::rk::partial_floats(d.sm_count)) *
+                                  sizeof(float);
+            const size_t sbytes = std::max(q4::tc::sem_ints(d.sm_count), q4::rk::sem_ints(d.sm_count)) * sizeof(int);
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * q4::prep::kRecordBytes);
@@ -233,6 +245,43 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
     return Q4_OK;
 }
 
+q4_status launch_rk(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                    cudaStream_t stream) {
+    using namespace q4::rk;
+    CUtensorMap map_nib;
+    q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
+                            (uint64_t)K / 2, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (s != Q4_OK) return s;
+    Params p;
+    p.W = static_cast<const uint8_t*>(W);
+    p.xt = d.xt;
+    p.y = y;
+    p.partials = d.partials;
+    p.sems = d.sems;
+    p.error_word = d.error_word;
+    p.N = N;
+    p.K = K;
+    p.M = M;
+    p.G = (int)(K / 64);
+    p.T = (int)((N + kRowsTile - 1) / kRowsTile);
+    p.U = p.T * p.G;
+    p.C = p.U < d.sm_count ? p.U : d.sm_count;
+#ifdef Q4_TRACE
+    p.trace = g_trace;
+#endif
+    cudaError_t e = launch_pdl(q4::prep::prep_x_frag_kernel, dim3((unsigned)p.G), dim3(256), 0, stream,
+                               static_cast<const uint16_t*>(x), M, K, d.xt);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the x preparation kernel");
+    const dim3 grid((unsigned)p.C), block(kThreads);
+    const size_t smem = (size_t)smem_bytes();
+    if (M <= 8)
+        e = launch_pdl(q4_rk_kernel<1>, grid, block, smem, stream, map_nib, p);
+    else
+        e = launch_pdl(q4_rk_kernel<2>, grid, block, smem, stream, map_nib, p);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the register-operand Q4 kernel");
+    return Q4_OK;
+}
+
 // The launch plan depends on N, K and the device only -- never on M -- so a
 // row's result is the same for every M.
 bool use_tc(int64_t N, int64_t K) {
@@ -271,7 +320,15 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
     const DeviceInfo* info = nullptr;
     q4_status s = device_setup(&dev, &info);
     if (s != Q4_OK) return s;
-    if (use_tc(N, K)) return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+    if (use_tc(N, K)) {
+        // developer comparison switch: the register-operand kernel instead of the tensor-memory one
+        static const bool rk_kernel = [] {
+            const char* v = std::getenv("Q4_REGISTER_OPERAND_KERNEL");
+            return v && v[0] == '1';
+        }();
+        if (rk_kernel) return launch_rk(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+        return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+    }
     return launch_generic(x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -193,7 +193,9 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], int t, bool whole
 #pragma unroll
             for (int m = 0; m < MT; ++m) __stcg(dst + m * kRowsCG, acc[m]);
         }
-        __threadfence();
+        // the consumer group's partial stores are ordered before thread 0's
+        // release by the barrier; the last contributor's acquire makes every
+        // partial of the slice visible to its group after the second barrier
         named_barrier(1 + cg, kRowsCG);
         if (cg_tid == 0) {
             int last = 0;
@@ -202,9 +204,10 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], int t, bool whole
                 const int c_first = cta_of_unit(p.U, p.C, tu);
                 const int c_last = cta_of_unit(p.U, p.C, tu + p.G - 1);
                 int* sem = p.sems + c_first * kCG + cg;
-                const int old = atomicAdd(sem, 1);
+                int old;
+                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(sem) : "memory");
                 if (old == c_last - c_first) {
-                    atomicExch(sem, 0);      // leave the counter at zero for the next launch
+                    asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(sem) : "memory");   // zero for the next launch
                     last = 1;
                 }
             }
@@ -212,7 +215,6 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], int t, bool whole
         }
         named_barrier(1 + cg, kRowsCG);
         if (bcast[cg]) {
-            __threadfence();
             const int tu = t * p.G;
             finish_shared_slice<MT>(p, t, cg, row, cta_of_unit(p.U, p.C, tu), cta_of_unit(p.U, p.C, tu + p.G - 1));
         }
@@ -502,23 +504,30 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             const uint8_t* nb = smem + slot * kStageBytes + cg * kNibBox + row * 64;
             const int sx = (row >> 1) & 3;
             const uint32_t abase = tmem + lane_field + kColA + (uint32_t)((cg * 2 + (si & 1)) * 2 * 32);
+            // both groups' constants and nibbles, dequantized together (64 independent chains)
+            uint32_t cc0, cc1;
+            group_constants(s01[0], b0, r01[0], cc0);
+            group_constants(s01[1], b1, r01[1], cc1);
+            Q4_TR(p, tr + 8 * si + 1);
+            if (live) {
+                uint32_t a0[32], a1[32];
+                const uint4 n0 = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
+                const uint4 n1 = *reinterpret_cast<const uint4*>(nb + ((1 ^ sx) << 4));
+                const uint4 n2 = *reinterpret_cast<const uint4*>(nb + ((2 ^ sx) << 4));
+                const uint4 n3 = *reinterpret_cast<const uint4*>(nb + ((3 ^ sx) << 4));
+                dequant64(n0, n1, cc0, a0);
+                dequant64(n2, n3, cc1, a1);
+                tmem_st_32x32b_x32(abase, a0);
+                tmem_st_32x32b_x32(abase + 32, a1);
+            }
+            Q4_TR(p, tr + 8 * si + 2);
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
-                Q4_TR(p, tr + 8 * si + 1 + 3 * jj);
-                uint32_t cc;
-                group_constants(s01[jj], jj ? b1 : b0, r01[jj], cc);
-                if (live) {
-                    uint32_t a[32];
-                    dequant64(*reinterpret_cast<const uint4*>(nb + (((2 * jj) ^ sx) << 4)),
-                              *reinterpret_cast<const uint4*>(nb + (((2 * jj + 1) ^ sx) << 4)), cc, a);
-                    tmem_st_32x32b_x32(abase + 32 * jj, a);
-                }
-                Q4_TR(p, tr + 8 * si + 2 + 3 * jj);
                 // group jj of the previous stage, before its P buffer is reused
                 if (si > 0) fold_group(si - 1, jj);
-                Q4_TR(p, tr + 8 * si + 3 + 3 * jj);
+                Q4_TR(p, tr + 8 * si + 3 + jj);
                 if (live) {
-                    tmem_wait_st();                  // A is in tensor memory
+                    if (jj == 0) tmem_wait_st();     // A is in tensor memory
                     tc_fence_before();
                     mbar_arrive_relaxed(&ready[cg * 2 + jj]);
                 }
