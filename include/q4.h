@@ -70,7 +70,14 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
  *   W : device, packed buffer of exactly q4_packed_bytes(N, K) bytes, 16-byte aligned.
  *   M : 1..16 verify rows.   N : >= 1 outputs.   K : positive multiple of 64.
  *   y : device, fp32, row-major [M, N], 16-byte aligned; fully overwritten.
- * Allocates no device memory.
+ * Device memory: the first call on each device (with that device current)
+ * allocates the library's scratch -- split-K partial sums, per-tile counters
+ * and the prepared x records, about 14 MB on a 152-SM GPU -- and keeps it
+ * until the process exits; later calls allocate nothing.  Make that first
+ * call outside any stream capture.  Every call on a device shares this
+ * scratch, so calls that may run at the same time on one device (different
+ * streams without an ordering between them) race and give wrong results:
+ * order them on one stream or with events.
  * Accuracy: |y - exact| <= 2e-3 * sum_k |x[m,k] w[n,k]| per output. */
 q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     q4_stream_t stream);
