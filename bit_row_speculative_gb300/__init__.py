@@ -28,7 +28,8 @@ MAX_ROWS = 16
 GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).
-SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_device_status", "q4_last_error", "q4_status_string")
+SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_device_status", "q4_last_error",
+           "q4_status_string")
 
 
 class Q4Error(RuntimeError):
@@ -47,6 +48,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.q4_packed_bytes.argtypes = [c.c_uint64, c.c_uint64]
     lib.q4_matmul.restype = c.c_int
     lib.q4_matmul.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p]
+    lib.q4_matmul_noalloc.restype = c.c_int
+    lib.q4_matmul_noalloc.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p]
     lib.q4_device_status.restype = c.c_int
     lib.q4_device_status.argtypes = [c.c_void_p]
     lib.q4_last_error.restype = c.c_char_p
@@ -108,6 +111,26 @@ def matmul(x, W, N: int, K: int, y=None, stream=None):
     elif y.dtype != torch.float32 or tuple(y.shape) != (M, N) or not y.is_contiguous():
         raise ValueError("y must be a contiguous float32 [M, N] tensor")
     _check(lib().q4_matmul(x.data_ptr(), W.data_ptr(), M, N, K, y.data_ptr(), _stream_handle(stream)))
+    return y
+
+
+def matmul_noalloc(x, W, N: int, K: int, y, stream=None):
+    """q4_matmul_noalloc: the same product, with the library's fixed static
+    scratch instead of memory it allocates, for callers that may not allocate
+    device memory.  y must be given (a contiguous float32 [M, N] tensor)."""
+    import torch
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bfloat16 tensor")
+    if W.dtype != torch.uint8 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous uint8 tensor")
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError(f"x has {x.shape[1]} columns, K = {K}")
+    if W.numel() != packed_bytes(N, K):
+        raise ValueError(f"W has {W.numel()} bytes, expected {packed_bytes(N, K)}")
+    if y.dtype != torch.float32 or tuple(y.shape) != (M, N) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float32 [M, N] tensor")
+    _check(lib().q4_matmul_noalloc(x.data_ptr(), W.data_ptr(), M, N, K, y.data_ptr(), _stream_handle(stream)))
     return y
 
 

@@ -292,6 +292,106 @@ bool use_tc(int64_t N, int64_t K) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Scratch of q4_matmul_noalloc, for callers that may not allocate device
+// memory at run time.  It lives in the library's own image: every device that
+// loads the library holds kNoAllocScratchBytes of it until the process exits.
+// Layout: [split-K partial sums][per-tile counters][prepared x records], each
+// part 256-byte aligned, sized for the tensor-memory kernel with one CTA per
+// SM on up to kNoAllocMaxSms SMs and K up to kNoAllocMaxK.
+namespace {
+
+constexpr int kNoAllocMaxSms = 160;
+constexpr int64_t kNoAllocMaxK = 20480;
+constexpr size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+constexpr size_t kNoAllocPartialBytes =
+    round256((size_t)kNoAllocMaxSms * 2 * q4::tc::kCG * 16 * q4::tc::kRowsCG * sizeof(float));
+constexpr size_t kNoAllocSemBytes = round256((size_t)kNoAllocMaxSms * q4::tc::kCG * sizeof(int));
+constexpr size_t kNoAllocXtBytes = round256((size_t)(kNoAllocMaxK / 64) * q4::prep::kRecordBytes);
+constexpr size_t kNoAllocScratchBytes = kNoAllocPartialBytes + kNoAllocSemBytes + kNoAllocXtBytes;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char q4_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocDevice {
+    bool ready = false;
+    q4_status status = Q4_OK;
+    std::string error;
+    int sm_count = 0;
+    uint8_t* scratch = nullptr;          // device address of q4_noalloc_scratch on this device
+    unsigned int* error_word = nullptr;  // device address of q4_device_error_word
+};
+
+NoAllocDevice g_noalloc_devices[kMaxDevices];
+
+// One-time set-up of the current device for q4_matmul_noalloc: capability
+// check, kernel attributes and the device addresses of the static arrays.  In
+// host code the array's name only stands for it; the address a kernel needs
+// comes from cudaGetSymbolAddress with the device current.  Allocates nothing.
+q4_status noalloc_setup(const NoAllocDevice** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(Q4_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    NoAllocDevice& d = g_noalloc_devices[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        char buf[512];
+        if (prop.major != 10 || prop.minor != 3) {
+            d.status = Q4_ERR_UNSUPPORTED_DEVICE;
+            snprintf(buf, sizeof buf, "device %d (%s) is compute %d.%d; this library is built for 10.3 (sm_103a)",
+                     dev, prop.name, prop.major, prop.minor);
+            d.error = buf;
+        } else if (prop.multiProcessorCount > kNoAllocMaxSms) {
+            d.status = Q4_ERR_UNSUPPORTED_DEVICE;
+            snprintf(buf, sizeof buf,
+                     "device %d has %d SMs; the static scratch of q4_matmul_noalloc is sized for at most %d",
+                     dev, prop.multiProcessorCount, kNoAllocMaxSms);
+            d.error = buf;
+        } else {
+            d.sm_count = prop.multiProcessorCount;
+            cudaError_t a = prepare_generic<1>();
+            if (a == cudaSuccess) a = prepare_generic<2>();
+            if (a == cudaSuccess) a = prepare_generic<4>();
+            if (a == cudaSuccess) a = prepare_generic<8>();
+            if (a == cudaSuccess) a = prepare_generic<16>();
+            if (a == cudaSuccess) a = prepare_tc<1>();
+            if (a == cudaSuccess) a = prepare_tc<2>();
+            if (a == cudaSuccess) a = prepare_tc<4>();
+            if (a == cudaSuccess) a = prepare_tc<8>();
+            if (a == cudaSuccess) a = prepare_tc<16>();
+            if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
+            if (!g_encode) {
+                void* fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                a = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+                if (a != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                    return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+            }
+            void* ptr = nullptr;
+            a = cudaGetSymbolAddress(&ptr, q4_noalloc_scratch);
+            if (a != cudaSuccess) return cuda_fail(a, "cudaGetSymbolAddress(q4_noalloc_scratch)");
+            d.scratch = static_cast<uint8_t*>(ptr);
+            a = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), q4_device_error_word);
+            if (a != cudaSuccess) return cuda_fail(a, "cudaGetSymbolAddress(q4_device_error_word)");
+            d.status = Q4_OK;
+        }
+        d.ready = true;
+    }
+    if (d.status != Q4_OK) return fail(d.status, "%s", d.error.c_str());
+    *out = &d;
+    return Q4_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 uint64_t q4_packed_bytes(uint64_t N, uint64_t K) {
@@ -330,6 +430,42 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
         return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
     }
     return launch_generic(x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                            q4_stream_t stream) {
+    g_last_error.clear();
+    if (!x || !W || !y) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (x=%p W=%p y=%p)", x, W, (void*)y);
+    if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
+    if (N < 1) return fail(Q4_ERR_INVALID_ARG, "N = %lld must be >= 1", (long long)N);
+    if (K < 64 || (K % 64) != 0)
+        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "K = %lld must be a positive multiple of 64", (long long)K);
+    if (K > kNoAllocMaxK)
+        return fail(Q4_ERR_UNSUPPORTED_SHAPE,
+                    "K = %lld is larger than the %lld inputs the static scratch of q4_matmul_noalloc holds; "
+                    "use q4_matmul", (long long)K, (long long)kNoAllocMaxK);
+    if (q4_packed_bytes((uint64_t)N, (uint64_t)K) == 0)
+        return fail(Q4_ERR_OVERFLOW, "packed size of %lld x %lld overflows", (long long)N, (long long)K);
+    if ((uint64_t)M * (uint64_t)N > (1ull << 40))
+        return fail(Q4_ERR_INVALID_ARG, "output of %d x %lld is too large", M, (long long)N);
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y))
+        return fail(Q4_ERR_MISALIGNED, "x, W and y must be 16-byte aligned (x=%p W=%p y=%p)", x, W, (void*)y);
+    const NoAllocDevice* nd = nullptr;
+    q4_status s = noalloc_setup(&nd);
+    if (s != Q4_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!use_tc(N, K)) return launch_generic(x, W, M, N, K, y, st);   // this kernel needs no scratch
+    DeviceInfo view;
+    view.ready = true;
+    view.sm_count = nd->sm_count;
+    view.partials = reinterpret_cast<float*>(nd->scratch);
+    view.sems = reinterpret_cast<int*>(nd->scratch + kNoAllocPartialBytes);
+    view.xt = nd->scratch + kNoAllocPartialBytes + kNoAllocSemBytes;
+    view.error_word = nd->error_word;
+    // the counters must start at zero; a call that gave up a wait may have left them set
+    cudaError_t e = cudaMemsetAsync(view.sems, 0, kNoAllocSemBytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch counters");
+    return launch_tc(view, x, W, M, N, K, y, st);
 }
 
 q4_status q4_device_status(q4_stream_t stream) {

@@ -82,6 +82,29 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
 q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     q4_stream_t stream);
 
+/* q4_matmul for callers that must not allocate device memory.  The pages have
+ * no counterpart to this call; it exists for callers such as a serving
+ * engine that hands all free HBM to its own pools at start-up, a plug-in
+ * that runs inside a host application owning the device allocator, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.
+ *   Arguments, layout, result and accuracy are those of q4_matmul; the
+ *   caller still owns x, W and y.  K is limited to 20480 and the device to
+ *   160 SMs (larger: Q4_ERR_UNSUPPORTED_SHAPE / Q4_ERR_UNSUPPORTED_DEVICE,
+ *   nothing launched).
+ *   Scratch: a fixed array inside the library's device image (about 8.2 MB),
+ *   which every device that loads the library holds until the process exits.
+ *   No call allocates or frees device memory.  The first call on a device,
+ *   with that device current, looks up the array's device address and sets
+ *   kernel attributes; make that first call before any stream capture.
+ *   Every call clears the counters it needs at zero (an asynchronous memset
+ *   on `stream`) and overwrites the rest before reading it.
+ *   All calls on one device share the one array, so calls that may run at the
+ *   same time on the GPU (different streams with no ordering between them)
+ *   race and give wrong results: order them on one stream or with events. */
+q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                            q4_stream_t stream);
+
 /* Synchronizes `stream` and reports whether any kernel of this library on the
  * current device gave up a bounded device-side wait since the last query
  * (Q4_ERR_TIMEOUT), then clears that record.  Q4_OK otherwise. */
