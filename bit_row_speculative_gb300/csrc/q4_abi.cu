@@ -17,6 +17,7 @@
 #include "q4_generic.cuh"
 #include "q4_tc.cuh"
 #include "q4_mma.cuh"
+#include "q4_tm.cuh"
 
 // Set by a kernel whose bounded device-side wait ran out (never by a trap).
 __device__ unsigned int q4_device_error_word = 0;
@@ -49,6 +50,7 @@ struct DeviceInfo {
     float* partials = nullptr;      // split-K partial sums of the tensor-core kernel
     int* sems = nullptr;            // per-tile arrival counters (zero between launches)
     uint8_t* xt = nullptr;          // prepared x records (one per group of 64 inputs)
+    unsigned int* tm_state = nullptr;   // record flags [kTcMaxGroups], then the epoch and the finish count
     unsigned int* error_word = nullptr;
 };
 
@@ -77,6 +79,12 @@ template <int MT>
 cudaError_t prepare_tc() {
     return cudaFuncSetAttribute(q4::tc::q4_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 q4::tc::smem_bytes());
+}
+
+template <int MT>
+cudaError_t prepare_tm() {
+    return cudaFuncSetAttribute(q4::tm::q4_tm_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                q4::tm::smem_bytes());
 }
 
 template <int MT>
@@ -117,6 +125,11 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_tc<16>();
             if (a == cudaSuccess) a = prepare_rk<1>();
             if (a == cudaSuccess) a = prepare_rk<2>();
+            if (a == cudaSuccess) a = prepare_tm<1>();
+            if (a == cudaSuccess) a = prepare_tm<2>();
+            if (a == cudaSuccess) a = prepare_tm<4>();
+            if (a == cudaSuccess) a = prepare_tm<8>();
+            if (a == cudaSuccess) a = prepare_tm<16>();
             if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
             if (!g_encode) {
                 void* fn = nullptr;
@@ -127,12 +140,17 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
                 g_encode = reinterpret_cast<EncodeTiledFn>(fn);
             }
             // scratch of the tensor-core kernel, sized for one CTA per SM
-            const size_t pbytes = std::max(q4::tc::partial_floats(d.sm_count), q4::rk::partial_floats(d.sm_count)) *
+            const size_t pbytes = std::max({q4::tc::partial_floats(d.sm_count), q4::rk::partial_floats(d.sm_count),
+                                            q4::tm::partial_floats(d.sm_count)}) *
                                   sizeof(float);
-            const size_t sbytes = std::max(q4::tc::sem_ints(d.sm_count), q4::rk::sem_ints(d.sm_count)) * sizeof(int);
+            const size_t sbytes = std::max({q4::tc::sem_ints(d.sm_count), q4::rk::sem_ints(d.sm_count),
+                                            q4::tm::sem_ints(d.sm_count)}) *
+                                  sizeof(int);
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * q4::prep::kRecordBytes);
+            if (a == cudaSuccess) a = cudaMalloc(&d.tm_state, (size_t)(kTcMaxGroups + 2) * sizeof(unsigned int));
+            if (a == cudaSuccess) a = cudaMemset(d.tm_state, 0, (size_t)(kTcMaxGroups + 2) * sizeof(unsigned int));
             if (a == cudaSuccess) a = cudaMemset(d.sems, 0, sbytes);
             if (a == cudaSuccess) a = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), q4_device_error_word);
             if (a == cudaSuccess) a = cudaDeviceSynchronize();
@@ -245,19 +263,23 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
     return Q4_OK;
 }
 
-q4_status launch_rk(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     cudaStream_t stream) {
-    using namespace q4::rk;
+    using namespace q4::tm;
     CUtensorMap map_nib;
     q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
-                            (uint64_t)K / 2, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_64B);
+                            (uint64_t)K / 2, 64, kRowsCG, CU_TENSOR_MAP_SWIZZLE_64B);
     if (s != Q4_OK) return s;
     Params p;
     p.W = static_cast<const uint8_t*>(W);
-    p.xt = d.xt;
+    p.x = static_cast<const uint16_t*>(x);
     p.y = y;
     p.partials = d.partials;
     p.sems = d.sems;
+    p.xt = d.xt;
+    p.flags = d.tm_state;
+    p.epoch = d.tm_state + kTcMaxGroups;
+    p.finished = d.tm_state + kTcMaxGroups + 1;
     p.error_word = d.error_word;
     p.N = N;
     p.K = K;
@@ -269,11 +291,47 @@ q4_status launch_rk(const DeviceInfo& d, const void* x, const void* W, int M, in
 #ifdef Q4_TRACE
     p.trace = g_trace;
 #endif
-    cudaError_t e = launch_pdl(q4::prep::prep_x_frag_kernel, dim3((unsigned)p.G), dim3(256), 0, stream,
-                               static_cast<const uint16_t*>(x), M, K, d.xt);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the x preparation kernel");
     const dim3 grid((unsigned)p.C), block(kThreads);
     const size_t smem = (size_t)smem_bytes();
+    cudaError_t e;
+    switch (rows_template(M)) {
+        case 1: e = launch_pdl(q4_tm_kernel<1>, grid, block, smem, stream, map_nib, p); break;
+        case 2: e = launch_pdl(q4_tm_kernel<2>, grid, block, smem, stream, map_nib, p); break;
+        case 4: e = launch_pdl(q4_tm_kernel<4>, grid, block, smem, stream, map_nib, p); break;
+        case 8: e = launch_pdl(q4_tm_kernel<8>, grid, block, smem, stream, map_nib, p); break;
+        default: e = launch_pdl(q4_tm_kernel<16>, grid, block, smem, stream, map_nib, p); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "launching the tensor-memory Q4 kernel");
+    return Q4_OK;
+}
+
+q4_status launch_rk(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                    cudaStream_t stream) {
+    using namespace q4::rk;
+    CUtensorMap map_nib;
+    q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
+                            (uint64_t)K / 2, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (s != Q4_OK) return s;
+    Params p;
+    p.W = static_cast<const uint8_t*>(W);
+    p.x = static_cast<const uint16_t*>(x);
+    p.y = y;
+    p.partials = d.partials;
+    p.sems = d.sems;
+    p.error_word = d.error_word;
+    p.N = N;
+    p.K = K;
+    p.M = M;
+    p.G = (int)(K / 64);
+    p.T = (int)((N + kRowsTile - 1) / kRowsTile);
+    p.U = p.T * (p.G / 2);
+    p.C = p.U < d.sm_count ? p.U : d.sm_count;
+#ifdef Q4_TRACE
+    p.trace = g_trace;
+#endif
+    const dim3 grid((unsigned)p.C), block(kThreads);
+    const size_t smem = (size_t)smem_bytes();
+    cudaError_t e;
     if (M <= 8)
         e = launch_pdl(q4_rk_kernel<1>, grid, block, smem, stream, map_nib, p);
     else
@@ -421,13 +479,14 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
     q4_status s = device_setup(&dev, &info);
     if (s != Q4_OK) return s;
     if (use_tc(N, K)) {
-        // developer comparison switch: the register-operand kernel instead of the tensor-memory one
-        static const bool rk_kernel = [] {
-            const char* v = std::getenv("Q4_REGISTER_OPERAND_KERNEL");
-            return v && v[0] == '1';
+        // developer comparison switch: 1 = two-launch tensor-memory kernel, 2 = register-operand kernel
+        static const int alt_kernel = [] {
+            const char* v = std::getenv("Q4_ALT_KERNEL");
+            return v ? std::atoi(v) : 0;
         }();
-        if (rk_kernel) return launch_rk(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
-        return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+        if (alt_kernel == 1) return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+        if (alt_kernel == 2) return launch_rk(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+        return launch_tm(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
     }
     return launch_generic(x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
 }
