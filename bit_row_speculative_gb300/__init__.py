@@ -28,8 +28,17 @@ MAX_ROWS = 16
 GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).
-SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_device_status", "q4_last_error",
-           "q4_status_string")
+SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_glue", "q4_decode_step_workspace_bytes",
+           "q4_decode_step", "q4_device_status", "q4_last_error", "q4_status_string")
+
+GLUE_NONE = 0
+GLUE_RMSNORM = 1
+GLUE_SWIGLU_RMSNORM = 2
+
+
+class Layer(ctypes.Structure):
+    """q4_layer: packed W [N, K] (device pointer) and the glue to the next layer."""
+    _fields_ = [("W", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("glue", ctypes.c_int)]
 
 
 class Q4Error(RuntimeError):
@@ -50,6 +59,13 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.q4_matmul.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p]
     lib.q4_matmul_noalloc.restype = c.c_int
     lib.q4_matmul_noalloc.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p]
+    lib.q4_glue.restype = c.c_int
+    lib.q4_glue.argtypes = [c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int, c.c_void_p, c.c_void_p]
+    lib.q4_decode_step_workspace_bytes.restype = c.c_size_t
+    lib.q4_decode_step_workspace_bytes.argtypes = [c.c_void_p, c.c_int, c.c_int]
+    lib.q4_decode_step.restype = c.c_int
+    lib.q4_decode_step.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p,
+                                   c.c_void_p]
     lib.q4_device_status.restype = c.c_int
     lib.q4_device_status.argtypes = [c.c_void_p]
     lib.q4_last_error.restype = c.c_char_p
@@ -132,6 +148,52 @@ def matmul_noalloc(x, W, N: int, K: int, y, stream=None):
         raise ValueError("y must be a contiguous float32 [M, N] tensor")
     _check(lib().q4_matmul_noalloc(x.data_ptr(), W.data_ptr(), M, N, K, y.data_ptr(), _stream_handle(stream)))
     return y
+
+
+def glue(y, K_next: int, kind: int, x_next=None, stream=None):
+    """q4_glue: x_next[M, K_next] (bf16) from y[M, N_prev] (fp32), both on the device."""
+    import torch
+    if y.dtype != torch.float32 or y.dim() != 2 or not y.is_contiguous():
+        raise ValueError("y must be a contiguous 2-D float32 tensor")
+    M, n_prev = y.shape
+    if x_next is None:
+        x_next = torch.empty((M, K_next), dtype=torch.bfloat16, device=y.device)
+    elif x_next.dtype != torch.bfloat16 or tuple(x_next.shape) != (M, K_next) or not x_next.is_contiguous():
+        raise ValueError("x_next must be a contiguous bfloat16 [M, K_next] tensor")
+    _check(lib().q4_glue(y.data_ptr(), M, n_prev, K_next, kind, x_next.data_ptr(), _stream_handle(stream)))
+    return x_next
+
+
+def _layer_array(layers):
+    """layers: sequence of (W tensor, N, K, glue) -> ctypes array of q4_layer."""
+    arr = (Layer * len(layers))()
+    for i, (W, N, K, g) in enumerate(layers):
+        arr[i] = Layer(W.data_ptr(), N, K, g)
+    return arr
+
+
+def decode_step_workspace_bytes(layers, M: int) -> int:
+    arr = _layer_array(layers)
+    return int(lib().q4_decode_step_workspace_bytes(ctypes.addressof(arr), len(layers), M))
+
+
+def decode_step(layers, x0, y_last=None, workspace=None, stream=None):
+    """q4_decode_step over `layers` = [(W, N, K, glue), ...] from x0 [M, K_0]
+    (bf16); returns y_last [M, N_last] (fp32).  The workspace (a uint8 device
+    tensor) is allocated here when not given."""
+    import torch
+    if x0.dtype != torch.bfloat16 or x0.dim() != 2 or not x0.is_contiguous():
+        raise ValueError("x0 must be a contiguous 2-D bfloat16 tensor")
+    M = x0.shape[0]
+    arr = _layer_array(layers)
+    need = int(lib().q4_decode_step_workspace_bytes(ctypes.addressof(arr), len(layers), M))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x0.device)
+    if y_last is None:
+        y_last = torch.empty((M, layers[-1][1]), dtype=torch.float32, device=x0.device)
+    _check(lib().q4_decode_step(ctypes.addressof(arr), len(layers), x0.data_ptr(), M, workspace.data_ptr(),
+                                workspace.numel(), y_last.data_ptr(), _stream_handle(stream)))
+    return y_last
 
 
 def matmul_raw(x_ptr: int, W_ptr: int, M: int, N: int, K: int, y_ptr: int, stream_handle: int) -> None:

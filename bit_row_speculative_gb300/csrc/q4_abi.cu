@@ -18,6 +18,7 @@
 #include "q4_tc.cuh"
 #include "q4_mma.cuh"
 #include "q4_tm.cuh"
+#include "q4_glue.cuh"
 
 // Set by a kernel whose bounded device-side wait ran out (never by a trap).
 __device__ unsigned int q4_device_error_word = 0;
@@ -348,6 +349,83 @@ bool use_tc(int64_t N, int64_t K) {
            ((N + q4::tc::kRowsTile - 1) / q4::tc::kRowsTile) * (K / 64) < ((int64_t)1 << 30);
 }
 
+// The kernel for a (validated) matmul: the tensor-memory kernel for K a
+// multiple of 512, the generic kernel otherwise.
+q4_status dispatch_matmul(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
+                          cudaStream_t stream) {
+    if (use_tc(N, K)) {
+        // developer comparison switch: 1 = two-launch tensor-memory kernel, 2 = register-operand kernel
+        static const int alt_kernel = [] {
+            const char* v = std::getenv("Q4_ALT_KERNEL");
+            return v ? std::atoi(v) : 0;
+        }();
+        if (alt_kernel == 1) return launch_tc(d, x, W, M, N, K, y, stream);
+        if (alt_kernel == 2) return launch_rk(d, x, W, M, N, K, y, stream);
+        return launch_tm(d, x, W, M, N, K, y, stream);
+    }
+    return launch_generic(x, W, M, N, K, y, stream);
+}
+
+// Argument checks shared by the matmul entry points (everything but the device).
+q4_status check_matmul_args(const void* x, const void* W, int M, int64_t N, int64_t K, const void* y) {
+    if (!x || !W || !y) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (x=%p W=%p y=%p)", x, W, y);
+    if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
+    if (N < 1) return fail(Q4_ERR_INVALID_ARG, "N = %lld must be >= 1", (long long)N);
+    if (K < 64 || (K % 64) != 0)
+        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "K = %lld must be a positive multiple of 64", (long long)K);
+    if (q4_packed_bytes((uint64_t)N, (uint64_t)K) == 0)
+        return fail(Q4_ERR_OVERFLOW, "packed size of %lld x %lld overflows", (long long)N, (long long)K);
+    if ((uint64_t)M * (uint64_t)N > (1ull << 40))
+        return fail(Q4_ERR_INVALID_ARG, "output of %d x %lld is too large", M, (long long)N);
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y))
+        return fail(Q4_ERR_MISALIGNED, "x, W and y must be 16-byte aligned (x=%p W=%p y=%p)", x, W, y);
+    return Q4_OK;
+}
+
+constexpr double kGlueEps = 1e-6;
+
+q4_status check_glue_args(const float* y, int M, int64_t n_prev, int64_t K, int kind, const void* x) {
+    if (!y || !x) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (y=%p x=%p)", (const void*)y, x);
+    if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
+    if (K < 1 || n_prev < 1) return fail(Q4_ERR_INVALID_ARG, "glue widths must be >= 1 (N_prev=%lld K=%lld)",
+                                         (long long)n_prev, (long long)K);
+    if (kind == Q4_GLUE_RMSNORM) {
+        if (K > n_prev)
+            return fail(Q4_ERR_INVALID_ARG, "RMSNORM glue takes the first K=%lld of N_prev=%lld columns", (long long)K,
+                        (long long)n_prev);
+    } else if (kind == Q4_GLUE_SWIGLU_RMSNORM) {
+        if (n_prev != 2 * K)
+            return fail(Q4_ERR_INVALID_ARG, "SWIGLU_RMSNORM glue needs N_prev == 2K (N_prev=%lld K=%lld)",
+                        (long long)n_prev, (long long)K);
+    } else {
+        return fail(Q4_ERR_INVALID_ARG, "unknown glue kind %d", kind);
+    }
+    if (!aligned16(y) || !aligned16(x))
+        return fail(Q4_ERR_MISALIGNED, "y and x must be 16-byte aligned (y=%p x=%p)", (const void*)y, x);
+    return Q4_OK;
+}
+
+q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind, void* x, cudaStream_t stream) {
+    cudaError_t e = launch_pdl(q4::glue::glue_kernel, dim3((unsigned)M), dim3(q4::glue::kThreads), 0, stream, y, n_prev,
+                               K, kind, kGlueEps, static_cast<uint16_t*>(x));
+    if (e != cudaSuccess) return cuda_fail(e, "launching the glue kernel");
+    return Q4_OK;
+}
+
+size_t round_up256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace of a decode step: one fp32 buffer for the widest intermediate y and
+// one bf16 buffer for the widest intermediate x.
+void decode_workspace_layout(const q4_layer* layers, int n_layers, int M, size_t* y_bytes, size_t* x_bytes) {
+    int64_t max_n = 0, max_k = 0;
+    for (int j = 0; j + 1 < n_layers; ++j) {
+        max_n = std::max(max_n, layers[j].N);
+        max_k = std::max(max_k, layers[j + 1].K);
+    }
+    *y_bytes = round_up256((size_t)M * (size_t)max_n * sizeof(float));
+    *x_bytes = round_up256((size_t)M * (size_t)max_k * sizeof(uint16_t));
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -463,32 +541,13 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K) {
 q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     q4_stream_t stream) {
     g_last_error.clear();
-    if (!x || !W || !y) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (x=%p W=%p y=%p)", x, W, (void*)y);
-    if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
-    if (N < 1) return fail(Q4_ERR_INVALID_ARG, "N = %lld must be >= 1", (long long)N);
-    if (K < 64 || (K % 64) != 0)
-        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "K = %lld must be a positive multiple of 64", (long long)K);
-    if (q4_packed_bytes((uint64_t)N, (uint64_t)K) == 0)
-        return fail(Q4_ERR_OVERFLOW, "packed size of %lld x %lld overflows", (long long)N, (long long)K);
-    if ((uint64_t)M * (uint64_t)N > (1ull << 40))
-        return fail(Q4_ERR_INVALID_ARG, "output of %d x %lld is too large", M, (long long)N);
-    if (!aligned16(x) || !aligned16(W) || !aligned16(y))
-        return fail(Q4_ERR_MISALIGNED, "x, W and y must be 16-byte aligned (x=%p W=%p y=%p)", x, W, (void*)y);
+    q4_status cs = check_matmul_args(x, W, M, N, K, y);
+    if (cs != Q4_OK) return cs;
     int dev = 0;
     const DeviceInfo* info = nullptr;
     q4_status s = device_setup(&dev, &info);
     if (s != Q4_OK) return s;
-    if (use_tc(N, K)) {
-        // developer comparison switch: 1 = two-launch tensor-memory kernel, 2 = register-operand kernel
-        static const int alt_kernel = [] {
-            const char* v = std::getenv("Q4_ALT_KERNEL");
-            return v ? std::atoi(v) : 0;
-        }();
-        if (alt_kernel == 1) return launch_tc(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
-        if (alt_kernel == 2) return launch_rk(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
-        return launch_tm(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
-    }
-    return launch_generic(x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
+    return dispatch_matmul(*info, x, W, M, N, K, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
@@ -525,6 +584,87 @@ q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int6
     cudaError_t e = cudaMemsetAsync(view.sems, 0, kNoAllocSemBytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch counters");
     return launch_tc(view, x, W, M, N, K, y, st);
+}
+
+q4_status q4_glue(const float* y, int M, int64_t n_prev, int64_t k_next, int kind, void* x_next,
+                  q4_stream_t stream) {
+    g_last_error.clear();
+    q4_status s = check_glue_args(y, M, n_prev, k_next, kind, x_next);
+    if (s != Q4_OK) return s;
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    return launch_glue(y, M, n_prev, k_next, kind, x_next, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t q4_decode_step_workspace_bytes(const q4_layer* layers, int n_layers, int M) {
+    if (!layers || n_layers < 1 || M < 1 || M > Q4_MAX_ROWS) return 0;
+    size_t yb = 0, xb = 0;
+    decode_workspace_layout(layers, n_layers, M, &yb, &xb);
+    return yb + xb;
+}
+
+q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, int M, void* workspace,
+                         size_t workspace_bytes, float* y_last, q4_stream_t stream) {
+    g_last_error.clear();
+    if (!layers || n_layers < 1) return fail(Q4_ERR_INVALID_ARG, "empty layer list (layers=%p n=%d)", (const void*)layers,
+                                            n_layers);
+    // the whole list is checked before anything is launched
+    for (int j = 0; j < n_layers; ++j) {
+        const q4_layer& L = layers[j];
+        // shapes and W of every layer; x0 and y_last stand in for the inner buffers (the workspace is checked below)
+        q4_status s = check_matmul_args(x0, L.W, M, L.N, L.K, y_last);
+        if (s != Q4_OK) {
+            std::string msg = g_last_error;
+            return fail(s, "layer %d: %s", j, msg.c_str());
+        }
+        if (j + 1 < n_layers) {
+            const q4_layer& Nx = layers[j + 1];
+            if (L.glue == Q4_GLUE_RMSNORM) {
+                if (Nx.K > L.N)
+                    return fail(Q4_ERR_INVALID_ARG, "layer %d: RMSNORM glue takes the first K=%lld of its N=%lld outputs",
+                                j, (long long)Nx.K, (long long)L.N);
+            } else if (L.glue == Q4_GLUE_SWIGLU_RMSNORM) {
+                if (L.N != 2 * Nx.K)
+                    return fail(Q4_ERR_INVALID_ARG, "layer %d: SWIGLU_RMSNORM glue needs N == 2 * next K (N=%lld K=%lld)",
+                                j, (long long)L.N, (long long)Nx.K);
+            } else {
+                return fail(Q4_ERR_INVALID_ARG, "layer %d: glue kind %d does not chain to layer %d", j, L.glue, j + 1);
+            }
+        }
+    }
+    size_t yb = 0, xb = 0;
+    decode_workspace_layout(layers, n_layers, M, &yb, &xb);
+    if (n_layers > 1) {
+        if (!workspace)
+            return fail(Q4_ERR_INVALID_ARG, "a %d-layer step needs a workspace of %zu bytes", n_layers, yb + xb);
+        if (!aligned16(workspace)) return fail(Q4_ERR_MISALIGNED, "workspace %p is not 16-byte aligned", workspace);
+        if (workspace_bytes < yb + xb)
+            return fail(Q4_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu bytes the step needs",
+                        workspace_bytes, yb + xb);
+    }
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    q4_status s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* ybuf = static_cast<float*>(workspace);
+    void* xbuf = static_cast<uint8_t*>(workspace) + yb;
+    const void* xj = x0;
+    for (int j = 0; j < n_layers; ++j) {
+        const q4_layer& L = layers[j];
+        const bool last = j + 1 == n_layers;
+        float* yj = last ? y_last : ybuf;
+        s = dispatch_matmul(*info, xj, L.W, M, L.N, L.K, yj, st);
+        if (s != Q4_OK) return s;
+        if (!last) {
+            s = launch_glue(yj, M, L.N, layers[j + 1].K, L.glue, xbuf, st);
+            if (s != Q4_OK) return s;
+            xj = xbuf;
+        }
+    }
+    return Q4_OK;
 }
 
 q4_status q4_device_status(q4_stream_t stream) {

@@ -105,6 +105,61 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
 q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                             q4_stream_t stream);
 
+/* How the output y_j of one layer of a chained verify pass becomes the input
+ * x_{j+1} of the next.  The pages' own between-layer operators (attention,
+ * Gated DeltaNet, gated norms) are outside the matmul path; this library joins
+ * layers with a fixed, bounded stand-in ("Splash engine" analysis, section
+ * "Everything in one command buffer": one submission runs every layer of the
+ * step in order):
+ *   RMSNORM:        v_k = y[m, k] for the first K_next columns (K_next <= N_prev)
+ *   SWIGLU_RMSNORM: v_k = silu(y[m, k]) * y[m, K_next + k]       (N_prev == 2 K_next)
+ *   x[m, k] = bf16_RNE( v_k / sqrt( mean_k v_k^2 + 1e-6 ) ),  silu(a) = a / (1 + e^-a)
+ * The sum of squares and the scaling are done in double, so the one rounding
+ * to bf16 matches an all-double evaluation except, rarely, where expf's
+ * single-precision rounding decides a tie-near value. */
+typedef enum {
+    Q4_GLUE_NONE = 0,              /* last layer: its y is the step's output  */
+    Q4_GLUE_RMSNORM = 1,
+    Q4_GLUE_SWIGLU_RMSNORM = 2
+} q4_glue_kind;
+
+/* One layer of a chained pass: packed W [N, K] (device, 16-byte aligned) and
+ * the glue that turns its output into the next layer's input. */
+typedef struct {
+    const void* W;
+    int64_t N;
+    int64_t K;
+    int glue;                      /* q4_glue_kind; ignored for the last layer */
+} q4_layer;
+
+/* The inter-layer step alone: x_next[M, K_next] (bf16, device) from y[M, N_prev]
+ * (fp32, device), as described above.  Both 16-byte aligned.  Asynchronous on
+ * `stream`; the kernel waits for the preceding kernel on the stream (it may be
+ * the matmul that writes y).  Provided so that a chained pass can be run and
+ * checked one layer at a time. */
+q4_status q4_glue(const float* y, int M, int64_t N_prev, int64_t K_next, int glue, void* x_next,
+                  q4_stream_t stream);
+
+/* Bytes of workspace q4_decode_step needs for this layer list and M: one fp32
+ * buffer for the widest intermediate output and one bf16 buffer for the widest
+ * intermediate input.  0 for an invalid list (or a single layer). */
+size_t q4_decode_step_workspace_bytes(const q4_layer* layers, int n_layers, int M);
+
+/* One decode step of the chained verify pass in one submission ("Splash
+ * engine", section "Everything in one command buffer"): for j = 0..n-1,
+ * y_j = x_j * W_j^T (as q4_matmul) and x_{j+1} = glue_j(y_j); the last layer
+ * writes y_last [M, N_{n-1}] (fp32, device, 16-byte aligned).  x0 is bf16
+ * [M, K_0] on the device.  Every kernel is chained with programmatic dependent
+ * launch, so layer j+1 starts streaming its weights while layer j finishes.
+ * The whole list is checked before anything is launched (Q4_ERR_INVALID_ARG
+ * names the first bad layer); `workspace` (device, 16-byte aligned, at least
+ * q4_decode_step_workspace_bytes) holds the intermediates and must not overlap
+ * x0 or y_last.  Asynchronous on `stream`; the same scratch rules as q4_matmul
+ * apply, and the call may be captured in a CUDA graph once the device has been
+ * set up by an earlier call. */
+q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, int M, void* workspace,
+                         size_t workspace_bytes, float* y_last, q4_stream_t stream);
+
 /* Synchronizes `stream` and reports whether any kernel of this library on the
  * current device gave up a bounded device-side wait since the last query
  * (Q4_ERR_TIMEOUT), then clears that record.  Q4_OK otherwise. */

@@ -64,3 +64,62 @@ def test_argument_errors_return_before_launch(args, status):
     rc = lib.q4_matmul(*args, None)
     assert rc == status, (rc, lib.q4_last_error())
     assert lib.q4_last_error().decode() != ""
+
+
+def _layers(spec):
+    """ctypes q4_layer array from (W address, N, K, glue) tuples."""
+    arr = (q4.Layer * len(spec))()
+    for i, (w, N, K, g) in enumerate(spec):
+        arr[i] = q4.Layer(w, N, K, g)
+    return arr
+
+
+def test_decode_workspace_size():
+    lib = q4.lib()
+    spec = [(16, 2048, 512, q4.GLUE_SWIGLU_RMSNORM), (16, 1280, 1024, q4.GLUE_RMSNORM), (16, 300, 576, q4.GLUE_NONE)]
+    arr = _layers(spec)
+    need = lib.q4_decode_step_workspace_bytes(ctypes.addressof(arr), 3, 16)
+    # widest intermediate y: 16 x 2048 fp32; widest intermediate x: 16 x 1024 bf16 (each rounded to 256 bytes)
+    assert need == 16 * 2048 * 4 + 16 * 1024 * 2
+    assert lib.q4_decode_step_workspace_bytes(ctypes.addressof(arr), 1, 16) == 0
+    assert lib.q4_decode_step_workspace_bytes(None, 3, 16) == 0
+    assert lib.q4_decode_step_workspace_bytes(ctypes.addressof(arr), 3, 17) == 0
+
+
+@pytest.mark.parametrize("spec,ws,status", [
+    ([(16, 2000, 512, q4.GLUE_SWIGLU_RMSNORM), (16, 300, 1000, q4.GLUE_NONE)], 1 << 20,
+     q4.Q4_ERR_UNSUPPORTED_SHAPE),                                              # K of layer 1 not a multiple of 64
+    ([(16, 2048, 512, q4.GLUE_SWIGLU_RMSNORM), (16, 300, 512, q4.GLUE_NONE)], 1 << 20,
+     q4.Q4_ERR_INVALID_ARG),                                                    # SwiGLU needs N == 2 * next K
+    ([(16, 2048, 512, q4.GLUE_RMSNORM), (16, 300, 4096, q4.GLUE_NONE)], 1 << 20,
+     q4.Q4_ERR_INVALID_ARG),                                                    # RMSNORM: next K > N
+    ([(16, 2048, 512, q4.GLUE_NONE), (16, 300, 512, q4.GLUE_NONE)], 1 << 20,
+     q4.Q4_ERR_INVALID_ARG),                                                    # no glue between layers
+    ([(16, 2048, 512, 7), (16, 300, 512, q4.GLUE_NONE)], 1 << 20,
+     q4.Q4_ERR_INVALID_ARG),                                                    # unknown glue kind
+    ([(16, 2048, 512, q4.GLUE_RMSNORM), (16, 300, 512, q4.GLUE_NONE)], 64,
+     q4.Q4_ERR_INVALID_ARG),                                                    # workspace too small
+    ([(16, 2048, 512, q4.GLUE_RMSNORM), (24, 300, 512, q4.GLUE_NONE)], 1 << 20,
+     q4.Q4_ERR_MISALIGNED),                                                     # W of layer 1 misaligned
+])
+def test_decode_step_rejects_bad_lists_before_launch(spec, ws, status):
+    lib = q4.lib()
+    buf = ctypes.create_string_buffer(256)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    arr = _layers([(p if w == 16 else p + 8, N, K, g) for w, N, K, g in spec])
+    rc = lib.q4_decode_step(ctypes.addressof(arr), len(spec), p, 4, p, ws, p, None)
+    assert rc == status, (rc, lib.q4_last_error())
+    assert lib.q4_last_error().decode() != ""
+
+
+@pytest.mark.parametrize("M,n_prev,K,kind,status", [
+    (4, 640, 700, q4.GLUE_RMSNORM, q4.Q4_ERR_INVALID_ARG),              # K > N_prev
+    (4, 640, 300, q4.GLUE_SWIGLU_RMSNORM, q4.Q4_ERR_INVALID_ARG),       # N_prev != 2K
+    (4, 640, 320, 3, q4.Q4_ERR_INVALID_ARG),                            # unknown kind
+    (0, 640, 320, q4.GLUE_RMSNORM, q4.Q4_ERR_INVALID_ARG),              # M = 0
+])
+def test_glue_rejects_bad_arguments(M, n_prev, K, kind, status):
+    lib = q4.lib()
+    buf = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    assert lib.q4_glue(p, M, n_prev, K, kind, p, None) == status

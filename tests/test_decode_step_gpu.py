@@ -1,0 +1,187 @@
+"""q4_decode_step and q4_glue on the GPU: the chained verify pass ("Splash
+engine" analysis, section "Everything in one command buffer": every layer of
+the step runs in order in one submission).
+
+Teacher-forced checks: each layer's GPU output is compared with the oracle
+applied to the GPU's own bf16 input of that layer, and each glue output with the
+oracle's glue of the GPU's own y.  The glue rounds once to bf16 from a value the
+GPU computes in double except for expf, so a rare 1-ulp difference from the
+all-double oracle is allowed (rate <= 1e-4, never more than 1 ulp).  The whole
+step through q4_decode_step must equal the layer-by-layer run bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import bit_row_speculative_gb300 as q4
+import oracle
+import synth_inputs as si
+from parity import check_tolerance, sample_columns, xbits
+
+pytestmark = pytest.mark.gpu
+
+GLUE_ULP_RATE = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def _rows_of(W: torch.Tensor, N: int, K: int, rows: np.ndarray) -> torch.Tensor:
+    """The packed matrix of the given output rows of W (gathered on W's device, returned on the CPU)."""
+    G = K // 64
+    idx = torch.as_tensor(rows, device=W.device, dtype=torch.long)
+    nib = W[: N * K // 2].view(N, K // 2)[idx]
+    sb = W[N * K // 2:].view(torch.bfloat16)
+    scales = sb[: N * G].view(N, G)[idx]
+    biases = sb[N * G:].view(N, G)[idx]
+    return si.pack_planes(nib.cpu(), scales.cpu(), biases.cpu())
+
+
+def _check_layer(x: torch.Tensor, W: torch.Tensor, N: int, K: int, y: torch.Tensor, cols, what: str):
+    """GPU y of one layer against the oracle on the GPU's own input x."""
+    if cols is None:
+        cols = np.arange(N)
+    Wsub = _rows_of(W, N, K, cols).numpy()
+    ref, scale = oracle.matmul(xbits(x), Wsub, len(cols), K)
+    check_tolerance(y.cpu().numpy()[:, cols], ref, scale, what)
+
+
+def _check_glue(y: torch.Tensor, K_next: int, kind: int, x_next: torch.Tensor, what: str):
+    """GPU glue output against the oracle's glue of the same fp32 y."""
+    ref = oracle.glue(y.cpu().numpy(), K_next, kind)
+    got = si.bf16_bits(x_next.cpu()).numpy().view(np.uint16)
+    diff = got != ref
+    if diff.any():
+        # 1 ulp in bf16 (same sign) and rare
+        d = np.abs(got[diff].astype(np.int32) - ref[diff].astype(np.int32))
+        assert int(d.max()) <= 1, f"{what}: glue differs from the oracle by {int(d.max())} ulp"
+        assert diff.mean() <= GLUE_ULP_RATE, f"{what}: glue 1-ulp differences at rate {diff.mean():.2e}"
+
+
+def _run_by_layers(layers, x0, checks=True, sample=None, tag=""):
+    """The chained pass one kernel at a time; returns the last y."""
+    x = x0
+    y = None
+    for j, (W, N, K, g) in enumerate(layers):
+        y = q4.matmul(x, W, N, K)
+        if checks:
+            cols = None if sample is None else sample_columns(N, sample, seed=N + K + j)
+            _check_layer(x, W, N, K, y, cols, f"{tag} layer {j} (N={N} K={K})")
+        if j + 1 < len(layers):
+            Kn = layers[j + 1][2]
+            x = q4.glue(y, Kn, g)
+            if checks:
+                _check_glue(y, Kn, g, x, f"{tag} glue {j}")
+    return y
+
+
+@pytest.mark.parametrize("kind,N_prev,K", [(q4.GLUE_RMSNORM, 640, 576), (q4.GLUE_RMSNORM, 5120, 5120),
+                                           (q4.GLUE_SWIGLU_RMSNORM, 2 * 17408, 17408),
+                                           (q4.GLUE_SWIGLU_RMSNORM, 2048, 1024)])
+def test_glue_against_oracle(kind, N_prev, K):
+    g = torch.Generator(device="cpu").manual_seed(N_prev + K)
+    y = (torch.randn((16, N_prev), generator=g) * 3.0).to(torch.float32)
+    x = q4.glue(y.cuda(), K, kind)
+    q4.device_status()
+    _check_glue(y, K, kind, x, f"glue kind {kind} {N_prev}->{K}")
+
+
+def test_glue_rows_are_independent():
+    y = torch.randn((16, 2048), generator=torch.Generator().manual_seed(5)).cuda()
+    full = si.bf16_bits(q4.glue(y, 1024, q4.GLUE_SWIGLU_RMSNORM).cpu())
+    for m in (0, 7, 15):
+        alone = si.bf16_bits(q4.glue(y[m:m + 1].contiguous(), 1024, q4.GLUE_SWIGLU_RMSNORM).cpu())
+        assert torch.equal(alone[0], full[m])
+
+
+def _small_chain(device="cuda"):
+    """Four layers with both glue kinds, a K that is not a multiple of 512 (the
+    generic kernel) and ragged N."""
+    spec = [(2048, 512, q4.GLUE_SWIGLU_RMSNORM), (1280, 1024, q4.GLUE_RMSNORM), (1024, 576, q4.GLUE_RMSNORM),
+            (300, 1024, q4.GLUE_NONE)]
+    return [(si.make_weights(N, K, 900 + i, device=device), N, K, g) for i, (N, K, g) in enumerate(spec)]
+
+
+@pytest.mark.parametrize("M", [1, 3, 16])
+def test_small_chain_teacher_forced(M):
+    layers = _small_chain()
+    x0 = si.make_x(M, 512, 950 + M, device="cuda")
+    y_layers = _run_by_layers(layers, x0, tag=f"M={M}")
+    y_step = q4.decode_step(layers, x0)
+    q4.device_status()
+    assert torch.equal(y_step, y_layers), "q4_decode_step differs from the same kernels run one at a time"
+
+
+def test_small_chain_rows_independent_of_M():
+    layers = _small_chain()
+    x16 = si.make_x(16, 512, 960, device="cuda")
+    y16 = q4.decode_step(layers, x16).cpu()
+    for M in (1, 2, 5, 8):
+        yM = q4.decode_step(layers, x16[:M].contiguous()).cpu()
+        assert torch.equal(yM, y16[:M]), f"M={M}"
+
+
+def test_decode_step_repeat_is_deterministic():
+    layers = _small_chain()
+    x = si.make_x(16, 512, 961, device="cuda")
+    first = q4.decode_step(layers, x).cpu()
+    ws = torch.empty(q4.decode_step_workspace_bytes(layers, 16), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        assert torch.equal(q4.decode_step(layers, x, workspace=ws).cpu(), first)
+
+
+def test_decode_step_in_a_cuda_graph():
+    """The step captured once and replayed gives the eager result for new inputs."""
+    layers = _small_chain()
+    x = si.make_x(16, 512, 962, device="cuda")
+    ws = torch.empty(q4.decode_step_workspace_bytes(layers, 16), dtype=torch.uint8, device="cuda")
+    y = torch.empty((16, 300), dtype=torch.float32, device="cuda")
+    q4.decode_step(layers, x, y_last=y, workspace=ws)          # device set-up outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q4.decode_step(layers, x, y_last=y, workspace=ws, stream=s)
+    for seed in (963, 964):
+        x.copy_(si.make_x(16, 512, seed, device="cuda"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = q4.decode_step(layers, x).cpu()
+        assert torch.equal(y.cpu(), ref)
+
+
+def _full_pass_layers(device="cuda"):
+    """The 27B-shaped pass: 64 layers (attention when i % 4 == 3, Gated DeltaNet
+    otherwise), each [in-proj, out-proj, gate/up, down], then the LM head twice."""
+    H, I = 5120, 17408
+    layers = []
+    for i in range(64):
+        attn = i % 4 == 3
+        n_in = 14336 if attn else 16640
+        k_out = 6144
+        spec = [(n_in, H, q4.GLUE_RMSNORM), (H, k_out, q4.GLUE_RMSNORM), (2 * I, H, q4.GLUE_SWIGLU_RMSNORM),
+                (H, I, q4.GLUE_RMSNORM)]
+        for t, (N, K, g) in enumerate(spec):
+            layers.append((si.make_weights(N, K, si.w_seed(5, 4 * i + t), device=device), N, K, g))
+    layers.append((si.make_weights(248320, H, si.w_seed(5, 256), device=device), 248320, H, q4.GLUE_RMSNORM))
+    layers.append((si.make_weights(248320, H, si.w_seed(5, 257), device=device), 248320, H, q4.GLUE_NONE))
+    return layers
+
+
+@pytest.mark.slow
+def test_full_27b_pass_teacher_forced():
+    """Every linear of the 64-layer pass and both LM-head calls, M=16: 512
+    sampled output columns per layer against the oracle on the GPU's own
+    inputs, every glue against the oracle, and the one-submission step equal to
+    the layer-by-layer run bit for bit."""
+    layers = _full_pass_layers()
+    total = sum(N * K * 9 // 16 for _, N, K, _ in layers)
+    assert total == 15_149_629_440
+    x0 = si.make_x(16, 5120, si.x_seed(5), device="cuda")
+    y_layers = _run_by_layers(layers, x0, sample=512, tag="27B")
+    y_step = q4.decode_step(layers, x0)
+    q4.device_status()
+    assert torch.equal(y_step, y_layers)
