@@ -8,7 +8,12 @@ graph and replayed.  value = algorithmic HBM bytes of the step / device time,
 bytes per call = N*K*0.5625 + M*K*2 + M*N*4 (weights once, x once, y once).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload attn_sweep|lm_head|mlp_gdn]
+                    [--workload attn_sweep|lm_head|mlp_gdn|full_pass]
+
+full_pass: one step = the whole 27B-shaped verify pass through q4_decode_step
+(64 layers x [in-proj, out-proj, gate/up, down] + the LM head twice, M = 16,
+glue between layers), captured once in a CUDA graph; value = 15,149,629,440
+weight bytes + activations and outputs per step / device time.
 
 Under torchrun each rank runs its own replica (the path needs no exchange);
 rank 0 prints one JSON line with the max-over-ranks time.
@@ -39,7 +44,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["attn_sweep", "lm_head", "mlp_gdn"], default="attn_sweep")
+    p.add_argument("--workload", choices=["attn_sweep", "lm_head", "mlp_gdn", "full_pass"], default="attn_sweep")
     p.add_argument("--reps", type=int, default=20, help="calls per M per step")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -55,8 +60,31 @@ def workload_spec(name):
     if name == "lm_head":
         N, K = si.SHAPES["lm_head"]
         return [("lm_head", N, K, [16, 16])], "LM head K=5120->N=248320, M=16, twice per step"
+    if name == "full_pass":
+        # the distinct linears of a GDN layer, M=16 (the CPU sample's shapes)
+        shapes = [(n, *si.SHAPES[n], [16]) for n in ("gdn_in", "gdn_out", "gate_up", "down")]
+        return shapes, ("full 27B-shaped verify pass: 64 layers (attention when i%4==3, else GDN) x [in-proj, "
+                        "out-proj, gate/up, down] + LM head x2, M=16, chained through q4_decode_step")
     shapes = [(n, *si.SHAPES[n], [1, 16]) for n in ("gate_up", "down", "gdn_in", "gdn_out")]
     return shapes, "MLP + GDN projections (gate/up, down, GDN in, GDN out), M=1 and 16"
+
+
+def max_over_ranks(value, world, device=None):
+    """The maximum of a per-rank float over all ranks (the slowest replica
+    sets the job time).  CPU tensor under gloo, device tensor under nccl."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    on = "cpu" if dist.get_backend() == "gloo" else device
+    t = torch.tensor([float(value)], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step_per_rank, steps, ms_max, world):
+    """Whole-job GB/s: the bytes every rank processed over the max-over-ranks time."""
+    return world * bytes_per_step_per_rank * steps / (ms_max / 1e3) / 1e9
 
 
 def call_bytes(M, N, K):
@@ -144,33 +172,43 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
+_CPU_INPUTS = {}
+
+
 def cpu_oracle_sample(spec, seconds, seed=0):
     """Time the CPU oracle on a bounded sample of the workload: every M of the
-    sweep over a subset of output columns; GB/s with the same byte formula."""
+    sweep over a run of output columns (the whole matrix, repeated, when the
+    host is fast enough), about `seconds` of wall time; GB/s with the same byte
+    formula as the GPU line."""
     import numpy as np
     import oracle
     import synth_inputs as si
     oracle.build()
     label, N, K, Ms = spec[0]
-    W = si.make_weights(N, K, 424242).numpy()
+    key = (N, K, tuple(Ms))
+    if key not in _CPU_INPUTS:                       # inputs made once per process, outside the timing
+        _CPU_INPUTS[key] = (si.make_weights(N, K, 424242).numpy(),
+                            {M: si.bf16_bits(si.make_x(M, K, 99 + M)).numpy().view(np.uint16) for M in set(Ms)})
+    W, xs = _CPU_INPUTS[key]
     threads = os.cpu_count() or 1
-    xs = {M: si.bf16_bits(si.make_x(M, K, 99 + M)).numpy().view(np.uint16) for M in set(Ms)}
-    # calibrate the column count on a small probe
-    probe = 64
+    # calibrate on a probe of 16 columns per thread
+    probe = min(N, 16 * threads)
     t0 = time.perf_counter()
     for M in Ms:
         oracle.matmul(xs[M], W, N, K, cols=np.arange(probe), threads=threads)
     dt = max(time.perf_counter() - t0, 1e-6)
-    ncols = int(min(N, max(probe, probe * seconds / dt)))
+    want = max(probe, int(probe * seconds / dt))
+    ncols, reps = (want, 1) if want <= N else (N, max(1, round(want / N)))
     cols = np.arange(ncols)
     t0 = time.perf_counter()
-    for M in Ms:
-        oracle.matmul(xs[M], W, N, K, cols=cols, threads=threads)
+    for _ in range(reps):
+        for M in Ms:
+            oracle.matmul(xs[M], W, N, K, cols=cols, threads=threads)
     el = time.perf_counter() - t0
-    nbytes = sum(call_bytes(M, ncols, K) for M in Ms)
+    nbytes = reps * sum(call_bytes(M, ncols, K) for M in Ms)
+    what = f"first {ncols} of {N} output columns" if reps == 1 else f"all {N} output columns, {reps} times"
     return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{label} K={K}, first {ncols} of {N} output columns, M in {Ms}, fp64 oracle, "
-                      f"{el:.1f} s wall"}
+            "sample": f"{label} K={K}, {what}, M in {Ms}, fp64 oracle on {threads} threads, {el:.1f} s wall"}
 
 
 def run_reference(args, rank, world):
@@ -179,15 +217,19 @@ def run_reference(args, rank, world):
         return
     spec, desc = workload_spec(args.workload)
     per_step = []
+    walls = []
     cb = None
     for _ in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         cb = cpu_oracle_sample(spec, max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))))
+        walls.append(time.perf_counter() - t0)
         per_step.append(cb["value"])
     vals = per_step[args.warmup:]
     value = statistics.mean(vals)
     label, N, K, Ms = spec[0]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.mean(walls[args.warmup:]), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": desc, "N": N, "K": K, "M": Ms},
             "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": value,
@@ -291,11 +333,8 @@ def run_ours(args, rank, world, local_rank):
 
     kernel_ms = sum(per_graph_ms.values())            # device time of the matmul calls only
     total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([kernel_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        kernel_ms = float(t.item())
-    value = world * step_bytes * args.steps / (kernel_ms / 1e3) / 1e9
+    kernel_ms = max_over_ranks(kernel_ms, world, dev)
+    value = job_throughput(step_bytes, args.steps, kernel_ms, world)
 
     per_m = {}
     for i, (label, N, K, M, g) in enumerate(graphs):
@@ -332,11 +371,8 @@ def run_ours(args, rank, world, local_rank):
             e1.record(stream)
         stream.synchronize()
         e_ms = e0.elapsed_time(e1) / e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(world * step_bytes / (e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": round(job_throughput(step_bytes, 1, e_ms, world), 1), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
 
     if rank != 0:
@@ -370,6 +406,124 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_full_pass(args, rank, world, local_rank):
+    """The chained 27B-shaped verify pass through q4_decode_step, M = 16."""
+    import torch
+    import bit_row_speculative_gb300 as q4
+    import synth_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    M = 16
+    spec = si.full_pass_spec()
+    _, desc = workload_spec("full_pass")
+    weight_bytes = sum(N * K * 9 // 16 for N, K, _ in spec)
+    n_mm = len(spec)
+    # algorithmic bytes of the step: every weight once, each layer's x and y once
+    step_bytes = sum(call_bytes(M, N, K) for N, K, _ in spec)
+    peak, peak_kind = read_peaks()
+    if rank == 0:
+        print(f"prediction: {step_bytes / 1e9:.3f} GB per step at {peak:.0f} GB/s ({peak_kind}) "
+              f"-> {step_bytes / peak / 1e6:.3f} ms per step floor", file=sys.stderr, flush=True)
+
+    layers = [(si.make_weights(N, K, si.w_seed(5, t) + 7 * rank, device=dev), N, K, g)
+              for t, (N, K, g) in enumerate(spec)]
+    x0 = si.make_x(M, spec[0][1], si.x_seed(5), device=dev)
+    y = torch.empty((M, spec[-1][0]), dtype=torch.float32, device=dev)
+    ws = torch.empty(q4.decode_step_workspace_bytes(layers, M), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            q4.decode_step(layers, x0, y_last=y, workspace=ws, stream=stream)
+    stream.synchronize()
+    q4.device_status(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        q4.decode_step(layers, x0, y_last=y, workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            g.replay()
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    q4.device_status(stream)
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    kernel_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_throughput(step_bytes, args.steps, kernel_ms, world)
+
+    # end to end through the public call: pinned host x0 -> device, the step,
+    # device y_last -> pinned host, every step
+    hx = x0.cpu().pin_memory()
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    dx = torch.empty_like(x0)
+    e_steps = max(1, min(args.steps, 5))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for s in range(e_steps + 1):
+            if s == 1:
+                e0.record(stream)
+            dx.copy_(hx, non_blocking=True)
+            q4.decode_step(layers, dx, y_last=y, workspace=ws, stream=stream)
+            hy.copy_(y, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+    e2e = {"value": round(job_throughput(step_bytes, 1, e_ms, world), 1), "unit": "GB/s",
+           "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hy.numel() * 4,
+           "ms_per_step": round(e_ms, 4)}
+
+    if rank != 0:
+        return
+    ms = kernel_ms / args.steps
+    achieved = step_bytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x, q4 weights, fp32 accumulate",
+        "data": "synthetic (seeded; nibbles uniform 0..15, scale |N(0,1)|*0.01, bias -8*scale+N(0,1e-3), x N(0,1))",
+        "config": {"workload": desc, "M": M, "layers": n_mm, "weight_bytes_per_step": weight_bytes,
+                   "l2": f"inputs ({weight_bytes / 1e9:.2f} GB of weights) far larger than L2 "
+                         f"({l2 / 2**20:.0f} MiB); one CUDA graph per step",
+                   "parallelism": f"replicas x{world}"},
+        "step_ms": {"median": round(statistics.median(step_ms), 4), "min": round(min(step_ms), 4),
+                    "max": round(max(step_ms), 4)},
+        "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": step_bytes // n_mm,
+                     "note": "whole step (matmul and glue launches) timed; a lower bound for the matmul kernel"},
+        "gpu_launches": (n_mm + (n_mm - 1)) * args.steps,
+        "clocks": clocks, "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_oracle_sample(workload_spec("full_pass")[0], args.cpu_seconds)
+        except Exception as exc:                     # report, do not hide
+            line["cpu_baseline"] = {"error": repr(exc)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -384,7 +538,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.workload == "full_pass":
+            run_full_pass(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

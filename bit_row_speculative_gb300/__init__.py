@@ -29,7 +29,7 @@ GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).
 SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_glue", "q4_decode_step_workspace_bytes",
-           "q4_decode_step", "q4_device_status", "q4_last_error", "q4_status_string")
+           "q4_decode_step", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
 
 GLUE_NONE = 0
 GLUE_RMSNORM = 1
@@ -66,6 +66,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.q4_decode_step.restype = c.c_int
     lib.q4_decode_step.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p,
                                    c.c_void_p]
+    lib.q4_check_wait_timeout.restype = c.c_int
+    lib.q4_check_wait_timeout.argtypes = [c.c_longlong, c.c_void_p]
     lib.q4_device_status.restype = c.c_int
     lib.q4_device_status.argtypes = [c.c_void_p]
     lib.q4_last_error.restype = c.c_char_p
@@ -199,6 +201,12 @@ def decode_step(layers, x0, y_last=None, workspace=None, stream=None):
 def matmul_raw(x_ptr: int, W_ptr: int, M: int, N: int, K: int, y_ptr: int, stream_handle: int) -> None:
     """Pointer-level call of q4_matmul (for callers that manage their own buffers)."""
     _check(lib().q4_matmul(x_ptr, W_ptr, M, N, K, y_ptr, stream_handle))
+
+
+def check_wait_timeout(limit_cycles: int, stream=None) -> None:
+    """Launch the timeout self-check: a bounded wait that runs out after
+    `limit_cycles` and is then reported by device_status()."""
+    _check(lib().q4_check_wait_timeout(int(limit_cycles), _stream_handle(stream)))
 
 
 def device_status(stream=None) -> None:

@@ -25,6 +25,22 @@ __device__ unsigned int q4_device_error_word = 0;
 
 namespace {
 
+constexpr unsigned int kErrWaitCheck = 0x80000000u;   // bit set by the wait self-check below
+
+// One thread waits, with the kernels' own bounded wait, on an mbarrier that
+// nothing arrives on; when the limit runs out it records a timeout in the
+// error word exactly as a kernel would, and returns.
+__global__ void wait_check_kernel(long long limit_cycles, unsigned int* error_word) {
+    __shared__ uint64_t bar;
+    q4::sm100::mbar_init(&bar, 1);
+    q4::sm100::fence_mbar_init();
+    if (!q4::sm100::mbar_wait(&bar, 0, limit_cycles)) atomicOr(error_word, kErrWaitCheck);
+}
+
+}  // namespace
+
+namespace {
+
 thread_local std::string g_last_error;
 
 q4_status fail(q4_status s, const char* fmt, ...) {
@@ -664,6 +680,20 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
             xj = xbuf;
         }
     }
+    return Q4_OK;
+}
+
+q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream) {
+    g_last_error.clear();
+    if (limit_cycles < 1 || limit_cycles > (1ll << 32))
+        return fail(Q4_ERR_INVALID_ARG, "limit_cycles must be in 1..2^32 (got %lld)", limit_cycles);
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    q4_status s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    wait_check_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_cycles, info->error_word);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launching the wait check");
     return Q4_OK;
 }
 

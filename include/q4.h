@@ -160,6 +160,15 @@ size_t q4_decode_step_workspace_bytes(const q4_layer* layers, int n_layers, int 
 q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, int M, void* workspace,
                          size_t workspace_bytes, float* y_last, q4_stream_t stream);
 
+/* Self-check of the timeout reporting path.  Launches one thread on `stream`
+ * that waits, with the same bounded wait every kernel of this library uses, on
+ * a barrier that nothing signals; after `limit_cycles` SM clock cycles
+ * (1..2^32) it records the timeout in the device error word, as a kernel whose
+ * wait ran out does, and exits normally -- no trap, the context stays usable.
+ * The next q4_device_status() then returns Q4_ERR_TIMEOUT and clears the
+ * record.  Asynchronous; Q4_ERR_INVALID_ARG for a limit out of range. */
+q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream);
+
 /* Synchronizes `stream` and reports whether any kernel of this library on the
  * current device gave up a bounded device-side wait since the last query
  * (Q4_ERR_TIMEOUT), then clears that record.  Q4_OK otherwise. */

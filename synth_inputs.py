@@ -97,3 +97,17 @@ SHAPES = {
     "attn_out": (HIDDEN, ATTN_OUT_IN),
     "lm_head": (VOCAB, HIDDEN),
 }
+
+
+def full_pass_spec():
+    """(N, K, glue) of every linear of the 27B-shaped verify pass, in order: 64
+    layers (attention when i % 4 == 3, Gated DeltaNet otherwise, the page's
+    fullAttentionPeriod of 4), each [in-proj, out-proj, gate/up, down], then the
+    LM head twice (target verify, draft readout).  glue: 1 = first K columns,
+    2 = SwiGLU halves, 0 = end of the step (the library's glue kinds)."""
+    spec = []
+    for i in range(64):
+        n_in = ATTN_IN if i % 4 == 3 else GDN_IN
+        spec += [(n_in, HIDDEN, 1), (HIDDEN, ATTN_OUT_IN, 1), (2 * INTERMEDIATE, HIDDEN, 2), (HIDDEN, INTERMEDIATE, 1)]
+    spec += [(VOCAB, HIDDEN, 1), (VOCAB, HIDDEN, 0)]
+    return spec

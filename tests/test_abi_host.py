@@ -123,3 +123,10 @@ def test_glue_rejects_bad_arguments(M, n_prev, K, kind, status):
     buf = ctypes.create_string_buffer(64)
     p = (ctypes.addressof(buf) + 15) & ~15
     assert lib.q4_glue(p, M, n_prev, K, kind, p, None) == status
+
+
+@pytest.mark.parametrize("limit", [0, -5, (1 << 32) + 1])
+def test_wait_check_rejects_bad_limits(limit):
+    lib = q4.lib()
+    assert lib.q4_check_wait_timeout(limit, None) == q4.Q4_ERR_INVALID_ARG
+    assert "limit_cycles" in lib.q4_last_error().decode()

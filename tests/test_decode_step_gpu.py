@@ -156,19 +156,8 @@ def test_decode_step_in_a_cuda_graph():
 def _full_pass_layers(device="cuda"):
     """The 27B-shaped pass: 64 layers (attention when i % 4 == 3, Gated DeltaNet
     otherwise), each [in-proj, out-proj, gate/up, down], then the LM head twice."""
-    H, I = 5120, 17408
-    layers = []
-    for i in range(64):
-        attn = i % 4 == 3
-        n_in = 14336 if attn else 16640
-        k_out = 6144
-        spec = [(n_in, H, q4.GLUE_RMSNORM), (H, k_out, q4.GLUE_RMSNORM), (2 * I, H, q4.GLUE_SWIGLU_RMSNORM),
-                (H, I, q4.GLUE_RMSNORM)]
-        for t, (N, K, g) in enumerate(spec):
-            layers.append((si.make_weights(N, K, si.w_seed(5, 4 * i + t), device=device), N, K, g))
-    layers.append((si.make_weights(248320, H, si.w_seed(5, 256), device=device), 248320, H, q4.GLUE_RMSNORM))
-    layers.append((si.make_weights(248320, H, si.w_seed(5, 257), device=device), 248320, H, q4.GLUE_NONE))
-    return layers
+    return [(si.make_weights(N, K, si.w_seed(5, t), device=device), N, K, g)
+            for t, (N, K, g) in enumerate(si.full_pass_spec())]
 
 
 @pytest.mark.slow
