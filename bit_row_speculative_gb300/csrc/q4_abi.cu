@@ -67,7 +67,6 @@ struct DeviceInfo {
     float* partials = nullptr;      // split-K partial sums of the tensor-core kernel
     int* sems = nullptr;            // per-tile arrival counters (zero between launches)
     uint8_t* xt = nullptr;          // prepared x records (one per group of 64 inputs)
-    unsigned int* tm_state = nullptr;   // record flags [kTcMaxGroups], then the epoch and the finish count
     unsigned int* error_word = nullptr;
 };
 
@@ -166,8 +165,6 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * q4::prep::kRecordBytes);
-            if (a == cudaSuccess) a = cudaMalloc(&d.tm_state, (size_t)(kTcMaxGroups + 2) * sizeof(unsigned int));
-            if (a == cudaSuccess) a = cudaMemset(d.tm_state, 0, (size_t)(kTcMaxGroups + 2) * sizeof(unsigned int));
             if (a == cudaSuccess) a = cudaMemset(d.sems, 0, sbytes);
             if (a == cudaSuccess) a = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), q4_device_error_word);
             if (a == cudaSuccess) a = cudaDeviceSynchronize();
@@ -285,32 +282,31 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
     using namespace q4::tm;
     CUtensorMap map_nib;
     q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
-                            (uint64_t)K / 2, 64, kRowsCG, CU_TENSOR_MAP_SWIZZLE_64B);
+                            (uint64_t)K / 2, 64, kRowsTile, CU_TENSOR_MAP_SWIZZLE_64B);
     if (s != Q4_OK) return s;
     Params p;
     p.W = static_cast<const uint8_t*>(W);
-    p.x = static_cast<const uint16_t*>(x);
     p.y = y;
     p.partials = d.partials;
     p.sems = d.sems;
     p.xt = d.xt;
-    p.flags = d.tm_state;
-    p.epoch = d.tm_state + kTcMaxGroups;
-    p.finished = d.tm_state + kTcMaxGroups + 1;
     p.error_word = d.error_word;
     p.N = N;
     p.K = K;
     p.M = M;
     p.G = (int)(K / 64);
+    p.GP = p.G / 2;
     p.T = (int)((N + kRowsTile - 1) / kRowsTile);
-    p.U = p.T * p.G;
+    p.U = p.T * p.GP;
     p.C = p.U < d.sm_count ? p.U : d.sm_count;
 #ifdef Q4_TRACE
     p.trace = g_trace;
 #endif
+    cudaError_t e = launch_pdl(xrec_kernel, dim3((unsigned)p.G), dim3(kRecThreads), 0, stream,
+                               static_cast<const uint16_t*>(x), M, K, d.xt);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the x record kernel");
     const dim3 grid((unsigned)p.C), block(kThreads);
     const size_t smem = (size_t)smem_bytes();
-    cudaError_t e;
     switch (rows_template(M)) {
         case 1: e = launch_pdl(q4_tm_kernel<1>, grid, block, smem, stream, map_nib, p); break;
         case 2: e = launch_pdl(q4_tm_kernel<2>, grid, block, smem, stream, map_nib, p); break;

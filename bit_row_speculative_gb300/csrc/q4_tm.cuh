@@ -1,4 +1,4 @@
-// Q4 verify-matmul kernel for sm_103a (K a multiple of 512): one launch per call.
+// Q4 verify-matmul kernel for sm_103a (K a multiple of 512).
 //
 // y[m,n] = sum_g ( s[n,g] * P[m,n,g] + r[n,g] * X[m,g] )
 //   P[m,n,g] = sum_{k in g} (q[n,k] - c[n,g]) * x[m,k]      (tensor core, exact products)
@@ -18,44 +18,49 @@
 // ones), so every tensor-core product is (q - c) * x * 2^-33 exactly and the
 // fold applies s * 2^33.  (|x| must stay below 2^28 for x * 2^100 to be finite.)
 //
-// One persistent CTA per SM, 16 warps; tiles of 384 rows, a stage is an
-// aligned pair of groups (inputs 128k .. 128k+127) of one tile.
-//   x records   once per call, each group's x record -- the M <= 16 rows of x
-//               for the group's 64 inputs in the tensor core's K-major
-//               core-matrix layout (inputs of each 8-block in the dequantized
-//               order k0 k4 k1 k5 k2 k6 k3 k7, scaled as above) and the group
-//               sums X -- is written to global scratch by one CTA (group g by
-//               CTA g mod C) and published with a per-launch epoch flag.  The
-//               epoch lives in device memory and advances when the last CTA of
-//               a launch finishes, so repeated launches (and graph replays)
-//               never mistake an older record for the current one.
-//   warp 0      producer: per stage three 128-row x 64-byte nibble boxes
-//               (TMA, 64-byte swizzle) into a 7-stage ring, then, once each
-//               group's flag shows the current epoch, a bulk copy of the
-//               stage's two x records into the same slot.
-//   warps 1..3  MMA issuers, one per consumer group: per stage 8 MMAs
-//               M128 N16 K16 (A = dequantized weights in tensor memory, B = the
-//               x records in shared memory, D = P in tensor memory).
-//   warps 4..15 three consumer groups of 4 warps; consumer group cg owns rows
-//               128*cg .. 128*cg+127 of the tile, one row per thread.  Per
-//               stage they dequantize the 2 x 64 nibbles of their row and store
-//               them to tensor memory (A double-buffered by stage), fold the
-//               previous stage's P into fp32 sums with s, r and X, and then
-//               hand the new A over (P has one buffer per group: the next MMAs
-//               are issued only after the fold has read it).
-// Work split: the T*G (tile, group) units are cut into equal contiguous
-// ranges, one per CTA (stream-K).  A tile whose groups span several CTAs is
+// Two kernels per call, chained by programmatic dependent launch:
+//   xrec_kernel  writes each group's 2112-byte x record to global scratch:
+//                the fp32 group sums X[0..15], then the M <= 16 rows of x for
+//                the group's 64 inputs as tensor-core core matrices (8 rows x
+//                8 inputs, 128 B each): rows 0-7 for the 8 input blocks, then
+//                rows 8-15.  Inputs of each 8-block are in the dequantized
+//                order k0 k4 k1 k5 k2 k6 k3 k7 and scaled as above; rows >= M
+//                are zero.  A kernel for M <= 8 copies only the first 1088
+//                bytes (X and rows 0-7).
+//   q4_tm_kernel one persistent CTA per SM, 21 warps; tiles of 128 rows, a
+//                stage is two groups (128 inputs) of one tile.
+//     warp 0       producer: per stage one 128-row x 64-byte nibble box (TMA,
+//                  64-byte swizzle) into a ring of kStages slots, and bulk
+//                  copies of the two x records into the same slot.  The weight
+//                  boxes of the first kStages stages are issued before the
+//                  kernel waits for its predecessor (they need nothing from
+//                  it); every record copy comes after that wait.
+//     warps 1..4   MMA issuers, one per team: per stage of the team 8 MMAs
+//                  M128 N16 K16 (A = the dequantized weights in the team's
+//                  tensor memory, B = the x records in shared memory, D = the
+//                  team's P) and a commit to the team's "done" barrier.
+//     warps 5..20  four consumer teams of 4 warps; stage i belongs to team
+//                  i % 4, so each team has four stage periods for its own
+//                  chain of waits, tensor-memory stores and loads.  The ring
+//                  has a multiple of 4 slots, so a slot always serves the same
+//                  team, and each barrier is waited on by threads that pass
+//                  through its phases in order (a parity wait never sees a
+//                  phase two steps away).
+//                  Every team covers all 128 rows (one row per thread): it
+//                  dequantizes the stage's 2 x 64 nibbles of the row into A,
+//                  hands A over, waits for the MMAs, folds P into its own
+//                  fp32 sums with s, r and X, and frees the slot.  At the end
+//                  of each tile segment the four teams' sums are added in
+//                  team order through shared memory.
+// Work split: the T*G/2 (tile, group pair) units are cut into equal contiguous
+// ranges, one per CTA (stream-K).  A tile whose units span several CTAs is
 // finished by the last of them to arrive, which adds the partial sums in
 // increasing CTA order.  The split depends only on N, K and the grid size, and
 // nothing in the arithmetic of row m depends on the other rows, so every
 // row's result is independent of M.
-// Programmatic dependent launch: the kernel lets the next kernel on the stream
-// start at once; the weight stream needs nothing from the preceding kernel.
-// Everything that touches x, y, the records or the split-K scratch waits for
-// the preceding kernel first (griddepcontrol.wait).  A CTA waits for another
-// CTA of the same launch only for a record flag; all CTAs of a launch fit on
-// the GPU at once, so such a wait ends unless other work holds the SMs, and it
-// is bounded in any case.
+// No CTA waits for another except through the last-arriver counter, which
+// never blocks.  Every barrier wait is bounded; a wait that runs out sets the
+// error word and the CTA runs to its end without further waiting.
 #pragma once
 
 #include <cuda.h>
@@ -66,31 +71,31 @@
 namespace q4 {
 namespace tm {
 
-constexpr int kCG = 3;                      // consumer groups
-constexpr int kRowsCG = 128;                // rows per consumer group (tensor-memory lanes)
-constexpr int kRowsTile = kCG * kRowsCG;    // 384 rows per tile
-constexpr int kStages = 7;
-constexpr int kThreads = 512;
-constexpr int kConsumerWarp0 = 4;
-constexpr int kConsumerWarps = kCG * 4;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kRegsControl = 56;
-constexpr int kRegsConsumer = 152;
-static_assert(128 * kRegsControl + kConsumerThreads * kRegsConsumer <= kThreads * 128,
-              "register split exceeds the launch");
+constexpr int kRowsTile = 128;              // rows per tile (tensor-memory lanes)
+constexpr int kTeams = 4;                   // consumer teams (one warpgroup each)
+// A multiple of kTeams: slot i % kStages then always belongs to team i % kTeams,
+// so every waiter on a slot's barriers has seen that slot's previous phase.
+constexpr int kStages = 12;
+static_assert(kStages % kTeams == 0, "each ring slot must belong to one team");
+constexpr int kIssuers = kTeams;            // one MMA issuer per team
+constexpr int kConsumerWarp0 = 1 + kIssuers;
+constexpr int kThreads = (kConsumerWarp0 + 4 * kTeams) * 32;   // 672
+constexpr int kConsumerThreads = kTeams * 128;
 
-constexpr int kRec = 2112;                            // x record of one group: 2048 B operand + 16 fp32 sums
-constexpr int kNibBox = kRowsCG * 64;                 // 8 KB: 128 rows x 64 B (two groups)
-constexpr int kNibStage = kCG * kNibBox;              // 24 KB
+constexpr int kRec = 2112;                            // x record of one group
+constexpr int kRecHalf = 1088;                        // X and rows 0-7
+constexpr int kRecB = 64;                             // offset of the core matrices in a record
+constexpr int kNibStage = kRowsTile * 64;             // 8 KB: 128 rows x 64 B (two groups)
 constexpr int kStageBytes = ((kNibStage + 2 * kRec + 1023) / 1024) * 1024;
+constexpr int kRedBytes = kTeams * 16 * kRowsTile * 4;   // team sums of one segment
 constexpr int kBarrierBytes = 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024 /* alignment slack */;
+constexpr int kSmemBytes = kStages * kStageBytes + kRedBytes + kBarrierBytes + 1024 /* alignment slack */;
 
-// tensor-memory columns: A [cg][stage parity][group] x 32, P [cg][group] x 16
-constexpr uint32_t kColA = 0;
-constexpr uint32_t kColP = kColA + kCG * 2 * 2 * 32;
+// tensor-memory columns per team: A (two groups x 32), P (two groups x 16)
+constexpr uint32_t kColsTeam = 96;
+constexpr uint32_t kColP = 64;
 constexpr uint32_t kTmemCols = 512;
-static_assert(kColP + kCG * 2 * 16 <= kTmemCols, "tensor memory over-subscribed");
+static_assert(kTeams * kColsTeam <= kTmemCols, "tensor memory over-subscribed");
 
 constexpr long long kWaitLimit = 2000000000LL;     // cycles (about one second)
 constexpr float kFoldScale = 8589934592.0f;        // 2^33: undoes 2^-133 (weights) * 2^100 (x)
@@ -99,24 +104,21 @@ constexpr uint32_t kXScaleOdd = 0x6F806F80u;       // bf16 pair (2^96, 2^96)
 
 struct Params {
     const uint8_t* W;           // packed weights
-    const uint16_t* x;          // bf16 [M, K]
     float* y;                   // [M, N]
-    float* partials;            // scratch: [C][2][kCG][16][128]
-    int* sems;                  // scratch: [C][kCG], zero between launches
-    uint8_t* xt;                // scratch: x records [G][2112]
-    unsigned int* flags;        // scratch: [G] epoch of each group's record
-    unsigned int* epoch;        // scratch: launches completed (advanced by the last CTA)
-    unsigned int* finished;     // scratch: CTAs of the current launch that have finished
+    float* partials;            // scratch: [C][2][16][128]
+    int* sems;                  // scratch: [C], zero between launches
+    const uint8_t* xt;          // x records [G][2112] (written by xrec_kernel)
     unsigned int* error_word;   // set on a timed-out wait
     int64_t N;
     int64_t K;
     int M;
     int G;                      // K / 64 (a multiple of 8)
-    int T;                      // tiles of 384 rows
-    int U;                      // T * G units (groups of tiles)
+    int GP;                     // G / 2 group pairs (stages per tile)
+    int T;                      // tiles of 128 rows
+    int U;                      // T * GP units
     int C;                      // CTAs (grid size)
 #ifdef Q4_TRACE
-    unsigned long long* trace;  // developer timing trace of CTA 0 (compiled in only with Q4_TRACE)
+    unsigned long long* trace;  // developer timing trace (compiled in only with Q4_TRACE)
 #endif
 };
 
@@ -125,8 +127,20 @@ struct Params {
     do {                                                                                  \
         if ((p).trace && blockIdx.x == 0 && (idx) < 4096) (p).trace[(idx)] = clock64(); \
     } while (0)
+// globaltimer (ns) of any CTA, for start/end skew across CTAs
+#define Q4_TMGT(p, idx)                                                                  \
+    do {                                                                                 \
+        if ((p).trace && (idx) < 4096) {                                                 \
+            unsigned long long gt_;                                                      \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(gt_));                      \
+            (p).trace[(idx)] = gt_;                                                      \
+        }                                                                                \
+    } while (0)
 #else
 #define Q4_TMTR(p, idx) \
+    do {                \
+    } while (0)
+#define Q4_TMGT(p, idx) \
     do {                \
     } while (0)
 #endif
@@ -201,106 +215,42 @@ __device__ __forceinline__ bool wait_or_abort(const Params& p, uint64_t* bar, ui
     return false;
 }
 
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* ptr) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
-}
+// ------------------------------------------------------------------ x records
+// One CTA per group of 64 inputs, 128 threads: thread t takes row m = t / 8
+// and 8-block kc = t % 8 of the group.
+constexpr int kRecThreads = 128;
 
-__device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
-}
-
-// Orders generic-proxy memory accesses with later async-proxy ones (TMA, bulk
-// copies, the tensor core) in every state space.
-__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
-
-// Bounded wait until the record flag of a group shows `target`.
-__device__ __forceinline__ bool wait_flag(const Params& p, const unsigned int* flag, unsigned int target,
-                                          volatile int* abort_flag) {
-    if (ld_acquire_gpu(flag) == target) return true;
-    const long long t0 = clock64();
-    while (ld_acquire_gpu(flag) != target) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimit) {
-            record_timeout(p, 32u, abort_flag);
-            return false;
-        }
-        __nanosleep(256);
+__global__ void __launch_bounds__(kRecThreads) xrec_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+                                                           uint8_t* __restrict__ xt) {
+    pdl_launch_dependents();
+    // x may come from the preceding kernel, and the preceding matmul may still
+    // read the records of its own call: wait for it first
+    pdl_wait();
+    const int g = blockIdx.x;
+    const int t = threadIdx.x;
+    const int m = t >> 3, kc = t & 7;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (m < M) v = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)m * K + (int64_t)g * 64 + kc * 8));
+    uint4 o;
+    o.x = bf16x2_mul(prmt(v.x, v.z, 0x5410u), kXScaleEven);    // (k0, k4)
+    o.y = bf16x2_mul(prmt(v.x, v.z, 0x7632u), kXScaleOdd);     // (k1, k5)
+    o.z = bf16x2_mul(prmt(v.y, v.w, 0x5410u), kXScaleEven);    // (k2, k6)
+    o.w = bf16x2_mul(prmt(v.y, v.w, 0x7632u), kXScaleOdd);     // (k3, k7)
+    uint8_t* rec = xt + (int64_t)g * kRec;
+    *reinterpret_cast<uint4*>(rec + kRecB + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
+    // X: the 8 inputs in increasing k, then the 8 block sums of the row (in 8
+    // consecutive lanes) by a fixed xor tree
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        s = __fadd_rn(s, __uint_as_float(w[i] << 16));
+        s = __fadd_rn(s, __uint_as_float(w[i] & 0xFFFF0000u));
     }
-    return true;
-}
-
-// Fixed-order finish of one 128-row slice of a tile whose groups span CTAs
-// [c_first, c_last]; run by the 128 threads of one consumer group of the last
-// CTA to arrive.
-template <int MT>
-__device__ void finish_shared_slice(const Params& p, int t, int cg, int row, int c_first, int c_last) {
-    const int64_t n = (int64_t)t * kRowsTile + cg * kRowsCG + row;
-    float acc[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
-    for (int c = c_first; c <= c_last; ++c) {
-        const int cs = range_start(p.U, p.C, c);
-        const int slot = (cs / p.G == t) ? 0 : 1;      // the tile is c's first segment, or its last
-        const float* src = p.partials + ((((int64_t)c * 2 + slot) * kCG + cg) * 16) * kRowsCG + row;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = __fadd_rn(acc[m], __ldcg(src + m * kRowsCG));
-    }
-    if (n < p.N) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-            if (m < p.M) p.y[(int64_t)m * p.N + n] = acc[m];
-    }
-}
-
-// End of this CTA's segment of tile t for one consumer group: store the sums
-// (whole tile), or publish them as a partial and let the last contributor add
-// all partials of the tile slice in increasing CTA order.
-template <int MT>
-__device__ void end_segment(const Params& p, float (&acc)[MT], int t, bool whole, int slot, int cg, int row,
-                            int cg_tid, int c_id, int* bcast, bool live) {
-    const int64_t n = (int64_t)t * kRowsTile + cg * kRowsCG + row;
-    if (whole) {
-        if (live && n < p.N) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < p.M) p.y[(int64_t)m * p.N + n] = acc[m];
-        }
-    } else {
-        float* dst = p.partials + ((((int64_t)c_id * 2 + slot) * kCG + cg) * 16) * kRowsCG + row;
-        if (live) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) __stcg(dst + m * kRowsCG, acc[m]);
-        }
-        // the consumer group's partial stores are ordered before thread 0's
-        // release by the barrier; the last contributor's acquire makes every
-        // partial of the slice visible to its group after the second barrier
-        named_barrier(1 + cg, kRowsCG);
-        if (cg_tid == 0) {
-            int last = 0;
-            if (live) {
-                const int tu = t * p.G;
-                const int c_first = cta_of_unit(p.U, p.C, tu);
-                const int c_last = cta_of_unit(p.U, p.C, tu + p.G - 1);
-                int* sem = p.sems + c_first * kCG + cg;
-                int old;
-                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(sem) : "memory");
-                if (old == c_last - c_first) {
-                    asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(sem) : "memory");   // zero for the next launch
-                    last = 1;
-                }
-            }
-            bcast[cg] = last;
-        }
-        named_barrier(1 + cg, kRowsCG);
-        if (bcast[cg]) {
-            const int tu = t * p.G;
-            finish_shared_slice<MT>(p, t, cg, row, cta_of_unit(p.U, p.C, tu), cta_of_unit(p.U, p.C, tu + p.G - 1));
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+    s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
+    s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
+    s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 4));
+    if (kc == 0) reinterpret_cast<float*>(rec)[m] = s;
 }
 
 // Dequantize the 64 nibbles of one row and group (two 16-byte chunks) into 32
@@ -335,23 +285,123 @@ __device__ __forceinline__ void group_constants(uint32_t s_bits, uint32_t b_bits
     cc0 = ci * 0x00010001u;
 }
 
-// One 8-input block of one row of x (natural order, bf16) into the tensor
-// core's order (k0,k4) (k1,k5) (k2,k6) (k3,k7) with the even inputs scaled by
-// 2^100 and the odd ones by 2^96 (exact); returns the fp32 sum of the 8
-// unscaled inputs, added in increasing k.
-__device__ __forceinline__ float x_block(const uint4& v, uint4& o) {
-    o.x = bf16x2_mul(prmt(v.x, v.z, 0x5410u), kXScaleEven);    // (k0, k4)
-    o.y = bf16x2_mul(prmt(v.x, v.z, 0x7632u), kXScaleOdd);     // (k1, k5)
-    o.z = bf16x2_mul(prmt(v.y, v.w, 0x5410u), kXScaleEven);    // (k2, k6)
-    o.w = bf16x2_mul(prmt(v.y, v.w, 0x7632u), kXScaleOdd);     // (k3, k7)
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float s = 0.0f;
+template <int MT>
+__device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, const float* xs, float s, float r) {
+    if (MT == 1) {
+        acc[0] = __fmaf_rn(s, __uint_as_float(P[0]), __fmaf_rn(r, xs[0], acc[0]));
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        s = __fadd_rn(s, __uint_as_float(w[i] << 16));
-        s = __fadd_rn(s, __uint_as_float(w[i] & 0xFFFF0000u));
+        for (int m4 = 0; m4 < (MT + 3) / 4; ++m4) {
+            float X[4];
+            if (MT >= 4) {
+                const float4 v = reinterpret_cast<const float4*>(xs)[m4];
+                X[0] = v.x;
+                X[1] = v.y;
+                X[2] = v.z;
+                X[3] = v.w;
+            } else {
+                X[0] = xs[0];
+                X[1] = xs[1];
+            }
+#pragma unroll
+            for (int i = 0; i < 4 && 4 * m4 + i + 1 < MT + 1; i += 2) {
+                const int m = 4 * m4 + i;
+                fma2(acc[m], acc[m + 1], r, X[i], X[i + 1]);
+                fma2(acc[m], acc[m + 1], s, __uint_as_float(P[m]), __uint_as_float(P[m + 1]));
+            }
+        }
     }
-    return s;
+}
+
+// End of a tile segment: the four teams' sums of rows [t*128, t*128+128) are
+// added in team order; a whole tile is stored, a partial one published and
+// finished by the last CTA to arrive (partials added in increasing CTA order).
+// Called by all 512 consumer threads; thread (team, row) handles m = team + 4j.
+template <int MT>
+__device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t, bool whole, int slot, int team,
+                            int row, int c_id, int* bcast, bool live) {
+    constexpr int kJ = (MT + 3) / 4;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) red[(team * 16 + m) * kRowsTile + row] = acc[m];
+    named_barrier(1, kConsumerThreads);
+    const int64_t n = (int64_t)t * kRowsTile + row;
+    float v[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+        const int m = team + 4 * j;
+        v[j] = 0.0f;
+        if (m < MT) {
+#pragma unroll
+            for (int tm_ = 0; tm_ < kTeams; ++tm_) v[j] = __fadd_rn(v[j], red[(tm_ * 16 + m) * kRowsTile + row]);
+        }
+    }
+    if (whole) {
+        if (live && n < p.N) {
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                const int m = team + 4 * j;
+                if (m < MT && m < p.M) p.y[(int64_t)m * p.N + n] = v[j];
+            }
+        }
+    } else {
+        float* dst = p.partials + (((int64_t)c_id * 2 + slot) * 16) * kRowsTile + row;
+        if (live) {
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                const int m = team + 4 * j;
+                if (m < MT) __stcg(dst + m * kRowsTile, v[j]);
+            }
+        }
+        // every thread makes its own partial stores visible device-wide before
+        // the barrier, so thread 0's counter increment follows all of them; the
+        // last contributor fences again after the barrier that follows its
+        // increment before any thread reads the other CTAs' partials
+        __threadfence();
+        named_barrier(1, kConsumerThreads);
+        const int tu = t * p.GP;
+        const int c_first = cta_of_unit(p.U, p.C, tu);
+        const int c_last = cta_of_unit(p.U, p.C, tu + p.GP - 1);
+        if (team == 0 && row == 0) {
+            int last = 0;
+            if (live) {
+                int* sem = p.sems + c_first;
+                int old;
+                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(sem) : "memory");
+                if (old == c_last - c_first) {
+                    asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(sem) : "memory");   // zero for the next launch
+                    last = 1;
+                }
+            }
+            *bcast = last;
+        }
+        named_barrier(1, kConsumerThreads);
+        if (*bcast) {
+            __threadfence();
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) v[j] = 0.0f;
+            for (int c = c_first; c <= c_last; ++c) {
+                const int cs = range_start(p.U, p.C, c);
+                const int cslot = (cs / p.GP == t) ? 0 : 1;   // the tile is c's first segment, or its last
+                const float* src = p.partials + (((int64_t)c * 2 + cslot) * 16) * kRowsTile + row;
+#pragma unroll
+                for (int j = 0; j < kJ; ++j) {
+                    const int m = team + 4 * j;
+                    if (m < MT) v[j] = __fadd_rn(v[j], __ldcg(src + m * kRowsTile));
+                }
+            }
+            if (n < p.N) {
+#pragma unroll
+                for (int j = 0; j < kJ; ++j) {
+                    const int m = team + 4 * j;
+                    if (m < MT && m < p.M) p.y[(int64_t)m * p.N + n] = v[j];
+                }
+            }
+        }
+    }
+    // red (and bcast) are rewritten at the next segment end only after every thread passed here
+    named_barrier(1, kConsumerThreads);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 }
 
 template <int MT>
@@ -360,40 +410,39 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     using namespace q4::sm100;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);   // nibbles and x records landed
-    uint64_t* empty = full + kStages;                  // stage consumed (nibbles, records, its folds): one arrival per issuer
-    uint64_t* ready = empty + kStages;                 // [kCG]: A of a stage stored
-    uint64_t* done = ready + kCG;                      // [kCG]: MMAs of a stage complete
-    uint64_t* fin = done + kCG;                        // [kCG]
-    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kCG);
+    float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kRedBytes);   // nibbles and records landed
+    uint64_t* empty = full + kStages;                  // slot free: the owning team has folded it
+    uint64_t* ready = empty + kStages;                 // [kTeams]: the team's A stored
+    uint64_t* done = ready + kTeams;                   // [kTeams]: the team's MMAs complete
+    uint64_t* fin = done + kTeams;                     // [kIssuers]
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
-    int* bcast = const_cast<int*>(abort_flag) + 1;     // [kCG]
+    int* bcast = const_cast<int*>(abort_flag) + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int c_id = blockIdx.x;
 
-    // the next kernel on the stream may start its own weight stream now
+    // the next kernel on the stream may start now
     pdl_launch_dependents();
 
-    // This CTA's units [u0, u1) and stages S0 .. S0+nst-1 (stage S = units 2S, 2S+1).
+    // This CTA's units (= stages) [u0, u1): unit u is group pair u % GP of tile u / GP.
     const int u0 = range_start(p.U, p.C, c_id);
     const int u1 = range_start(p.U, p.C, c_id + 1);
-    const int S0 = u0 >> 1;
-    const int nst = ((u1 - 1) >> 1) - S0 + 1;
-    const int Gh = p.G >> 1;
-    const int tS0 = S0 / Gh, kS0 = S0 - tS0 * Gh;      // tile and stage-in-tile of the first stage
+    const int nst = u1 - u0;
+    const int t0 = u0 / p.GP, gp0 = u0 - t0 * p.GP;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 2);
-            mbar_init(&empty[s], kCG);
+            mbar_init(&empty[s], 4);
         }
-        for (int i = 0; i < kCG; ++i) {
+        for (int i = 0; i < kTeams; ++i) {
             mbar_init(&ready[i], 4);
             mbar_init(&done[i], 1);
-            mbar_init(&fin[i], 1);
         }
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&fin[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -406,29 +455,22 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_slot;
-    if (threadIdx.x == 0) Q4_TMTR(p, 4000);
-
-    // Register split: the producer/issuer warpgroup needs few registers, the
-    // three consumer warpgroups many (128*56 + 384*152 = 512*128 at launch).
-    if (warp < kConsumerWarp0)
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-    else
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsumer));
+    if (threadIdx.x == 0) {
+        Q4_TMTR(p, 4000);
+        Q4_TMGT(p, 2400 + 2 * c_id);
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int tn = tS0, kn = kS0;                    // stage of the next nibble load
-            // one barrier per stage, two arrivals: the nibble boxes and the two x records, each with its bytes
+            int tn = t0, gn = gp0;                     // tile and group pair of the next nibble load
+            // one barrier per stage, two arrivals: the nibble box and the x records, each with its bytes
             auto issue_nibbles = [&](int slot) {
-                uint8_t* sbase = smem + slot * kStageBytes;
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)kNibStage);
-                for (int cg = 0; cg < kCG; ++cg)
-                    tma_load_2d_hint(sbase + cg * kNibBox, &map_nib, &full[slot], kn * 64,
-                                     tn * kRowsTile + cg * kRowsCG, pol);
-                if (++kn == Gh) {
-                    kn = 0;
+                tma_load_2d_hint(smem + slot * kStageBytes, &map_nib, &full[slot], gn * 64, tn * kRowsTile, pol);
+                if (++gn == p.GP) {
+                    gn = 0;
                     ++tn;
                 }
             };
@@ -436,9 +478,9 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             const int pre = nst < kStages ? nst : kStages;
             for (int si = 0; si < pre; ++si) issue_nibbles(si);
             int issued = pre, rec_issued = 0;
-            pdl_wait();
-            const unsigned int target = __ldcg(p.epoch) + 1u;
-            int kr = kS0;                              // stage-in-tile of the next record copy
+            pdl_wait();                                // the x records of this call are complete
+            Q4_TMTR(p, 4002);
+            int gr = gp0;                              // group pair of the next record copy
             int slot = 0;
             uint32_t ph = 0;
             for (int si = 0; si < nst; ++si) {
@@ -448,16 +490,18 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                     issue_nibbles(slot);
                     ++issued;
                 }
-                // the stage's two x records, once their writers have published them
-                const int g0 = 2 * kr;
-                if (!wait_flag(p, p.flags + g0, target, abort_flag) || !wait_flag(p, p.flags + g0 + 1, target, abort_flag))
-                    break;
-                fence_proxy_async_all();
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRec));
-                bulk_copy_g2s(smem + slot * kStageBytes + kNibStage, p.xt + (int64_t)g0 * kRec, (uint32_t)(2 * kRec),
-                              &full[slot]);
+                uint8_t* dst = smem + slot * kStageBytes + kNibStage;
+                const uint8_t* src = p.xt + (int64_t)(2 * gr) * kRec;
+                if (MT > 8) {
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRec));
+                    bulk_copy_g2s(dst, src, (uint32_t)(2 * kRec), &full[slot]);
+                } else {
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRecHalf));
+                    bulk_copy_g2s(dst, src, (uint32_t)kRecHalf, &full[slot]);
+                    bulk_copy_g2s(dst + kRec, src + kRec, (uint32_t)kRecHalf, &full[slot]);
+                }
                 ++rec_issued;
-                if (++kr == Gh) kr = 0;
+                if (++gr == p.GP) gr = 0;
                 if (++slot == kStages) {
                     slot = 0;
                     ph ^= 1u;
@@ -469,286 +513,167 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             for (int s2 = (issued > kStages ? issued - kStages : 0); s2 < issued; ++s2)
                 mbar_wait(&full[s2 % kStages], (s2 / kStages) & 1, kWaitLimit);
         }
-    } else if (warp <= kCG) {
+    } else if (warp <= kIssuers) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
-        const int cg = warp - 1;
+        const int iss = warp - 1;
         const uint32_t idesc = idesc_bf16_f32(128, 16);
-        const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(smem + kNibStage), 256, 128);
-        const uint32_t aA0 = tmem + kColA + (uint32_t)(cg * 4 * 32);
-        const uint32_t dP0 = tmem + kColP + (uint32_t)(cg * 2 * 16);
-        int slot = 0;
-        uint32_t ph = 0;
-        int uS = 2 * S0;
-        for (int si = 0; si < nst; ++si) {
-            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &full[slot], ph, 2u, abort_flag))) break;
-            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[cg], (uint32_t)(si & 1), 2u, abort_flag))) break;
+        // B: core matrices K-major, 128 B apart along K, rows 8-15 1024 B after rows 0-7
+        const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(smem + kNibStage + kRecB), 128, 1024);
+        const int team = iss;
+        for (int si = team; si < nst; si += kTeams) {
+            const int slot = si % kStages;
+            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 2u, abort_flag)))
+                break;
+            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)((si / kTeams) & 1), 2u,
+                                                       abort_flag)))
+                break;
             tc_fence_after();
-            // the consumer group has folded the previous stage: its ring slot is free as far as this group goes
-            if (si > 0 && lane == 0) mbar_arrive_relaxed(&empty[slot == 0 ? kStages - 1 : slot - 1]);
-            // operands computed by the whole warp (warp-uniform values), issued by one lane
-            const bool v0 = uS >= u0, v1 = uS + 1 < u1;
-            const uint64_t bd0 = bdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-            const uint64_t bd1 = bd0 + (uint64_t)(kRec >> 4);
-            const uint32_t aS = aA0 + (uint32_t)((si & 1) * 64);
+            const uint64_t bd = bdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
+            const uint32_t aS = tmem + (uint32_t)team * kColsTeam;
+            const uint32_t dS = aS + kColP;
             if (lane == 0) {
-                if (cg == 0) Q4_TMTR(p, 2000 + 2 * si);
-                if (v0) {
-                    tc_mma_ts(dP0, aS + 0u, bd0 + 0u, idesc, 0u);
-                    tc_mma_ts(dP0, aS + 8u, bd0 + 32u, idesc, 1u);
-                    tc_mma_ts(dP0, aS + 16u, bd0 + 64u, idesc, 1u);
-                    tc_mma_ts(dP0, aS + 24u, bd0 + 96u, idesc, 1u);
+                if (iss == 0) Q4_TMTR(p, 2000 + 2 * si);
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ts(dS + 16u * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
                 }
-                if (v1) {
-                    tc_mma_ts(dP0 + 16u, aS + 32u, bd1 + 0u, idesc, 0u);
-                    tc_mma_ts(dP0 + 16u, aS + 40u, bd1 + 32u, idesc, 1u);
-                    tc_mma_ts(dP0 + 16u, aS + 48u, bd1 + 64u, idesc, 1u);
-                    tc_mma_ts(dP0 + 16u, aS + 56u, bd1 + 96u, idesc, 1u);
-                }
-                tc_commit(&done[cg]);
-                if (cg == 0) Q4_TMTR(p, 2001 + 2 * si);
+                tc_commit(&done[team]);
+                if (iss == 0) Q4_TMTR(p, 2001 + 2 * si);
             }
             __syncwarp();
-            if (++slot == kStages) {
-                slot = 0;
-                ph ^= 1u;
-            }
-            uS += 2;
         }
         // no MMA of this warp may still run when tensor memory is freed
         if (lane == 0) {
-            tc_commit(&fin[cg]);
-            mbar_wait(&fin[cg], 0, kWaitLimit);
+            tc_commit(&fin[iss]);
+            mbar_wait(&fin[iss], 0, kWaitLimit);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ consumers
-        const int cw = warp - kConsumerWarp0;          // 0..11
-        const int cg = cw >> 2;
+        // ------------------------------------------------------------ consumer teams
+        const int team = (warp - kConsumerWarp0) >> 2;   // warps 5..8 team 0, ...; lane quarter = warp % 4
         const int q = warp & 3;                        // tensor-memory lane quarter of this warp
-        const int row = q * 32 + lane;                 // row within the consumer group's 128
-        const int ct = cw * 32 + lane;                 // 0..383 among the consumers
+        const int row = q * 32 + lane;                 // row within the tile
         const uint32_t lane_field = (uint32_t)(q * 32) << 16;
-        const uint32_t aA0 = tmem + lane_field + kColA + (uint32_t)(cg * 4 * 32);
-        const uint32_t dP0 = tmem + lane_field + kColP + (uint32_t)(cg * 2 * 16);
-        const int t_first = u0 / p.G;
-        [[maybe_unused]] const int tr = (lane == 0 && q == 0 && cg == 0) ? 1000 : 1 << 20;
+        const uint32_t aA = tmem + lane_field + (uint32_t)team * kColsTeam;
+        const uint32_t dP = aA + kColP;
+        [[maybe_unused]] const int tr = (lane == 0 && q == 0 && team == 0) ? 1000 : 1 << 20;
 
-        // scale and bias planes: per row 16-byte blocks of 8 groups (four stages)
+        // scale and bias planes: this team's two groups of a stage are one 4-byte word per plane
         const uint8_t* splane = p.W + p.N * (p.K / 2);
         const uint8_t* bplane = splane + p.N * p.G * 2;
-        const int rows_cg = cg * kRowsCG + row;
-        auto load_sb = [&](int t, int k, uint4& sv, uint4& bv) {   // block starting at stage-in-tile k of tile t
-            const int64_t n = (int64_t)t * kRowsTile + rows_cg;
-            if (n < p.N) {
-                const int64_t off = (n * p.G + 2 * k) * 2;
-                sv = __ldg(reinterpret_cast<const uint4*>(splane + off));
-                bv = __ldg(reinterpret_cast<const uint4*>(bplane + off));
+        auto load_sb = [&](int si, uint32_t& sv, uint32_t& bv) {
+            const int u = u0 + si;
+            const int t = u / p.GP, gp = u - t * p.GP;
+            const int64_t n = (int64_t)t * kRowsTile + row;
+            if (si < nst && n < p.N) {
+                const int64_t off = (n * p.G + 2 * gp) * 2;
+                sv = __ldg(reinterpret_cast<const uint32_t*>(splane + off));
+                bv = __ldg(reinterpret_cast<const uint32_t*>(bplane + off));
             } else {
-                sv = make_uint4(0, 0, 0, 0);
-                bv = make_uint4(0, 0, 0, 0);
+                sv = 0u;
+                bv = 0u;
             }
         };
-        uint4 cur_s, cur_b, nxt_s = make_uint4(0, 0, 0, 0), nxt_b = make_uint4(0, 0, 0, 0);
-        int k_sb = kS0 - (kS0 & 3), t_sb = tS0;        // block of the next load
-        int S_sb = S0 - (kS0 & 3);                     // its first stage
-        auto sb_next = [&]() {
-            k_sb += 4;
-            if (k_sb >= Gh) {
-                k_sb = 0;
-                ++t_sb;
-            }
-            S_sb += 4;
-        };
-        load_sb(t_sb, k_sb, cur_s, cur_b);
-        sb_next();
-        if (S_sb < S0 + nst) load_sb(t_sb, k_sb, nxt_s, nxt_b);
-
-        // x records of this CTA's groups (g = c_id, c_id + C, ...), published for every CTA
-        pdl_wait();                                    // x, the records, y and the split-K scratch
-        {
-            const unsigned int target = __ldcg(p.epoch) + 1u;
-            for (int g = c_id; g < p.G; g += p.C) {
-                if (ct < 128) {                        // 16 rows x 8 blocks of 8 inputs
-                    const int m = ct >> 3, c = ct & 7;
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (m < p.M) v = __ldg(reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + 64 * g + 8 * c));
-                    uint4 o;
-                    float s = x_block(v, o);
-                    uint8_t* rec = p.xt + (int64_t)g * kRec;
-                    *reinterpret_cast<uint4*>(rec + c * 256 + (m >> 3) * 128 + (m & 7) * 16) = o;
-                    // the 8 block sums of row m sit in 8 consecutive lanes: a fixed tree
-                    s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
-                    s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
-                    s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 4));
-                    if (c == 0) reinterpret_cast<float*>(rec + 2048)[m] = s;
-                }
-            }
-            fence_proxy_async_all();                   // the records are read by bulk copies
-            named_barrier(5, kConsumerThreads);
-            if (ct == 0) {
-                __threadfence();
-                for (int g = c_id; g < p.G; g += p.C) st_release_gpu(p.flags + g, target);
-            }
-        }
+        // scale/bias words of this team's next three stages (prefetched)
+        uint32_t s_a, b_a, s_b, b_b, s_c, b_c;
+        load_sb(team, s_a, b_a);
+        load_sb(team + kTeams, s_b, b_b);
+        load_sb(team + 2 * kTeams, s_c, b_c);
 
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
         bool live = true;
 
-        // the previous stage, folded during this one
-        int pslot = 0, pkst = 0, pt = 0, puS = -1;
-        float ps0 = 0.f, ps1 = 0.f, pr0 = 0.f, pr1 = 0.f;
-        auto fold_group = [&](int jj, const uint32_t* P, const float* xsum, float s, float r) {
-            float X[MT];
-            if (MT >= 4) {
-#pragma unroll
-                for (int v4 = 0; v4 < MT / 4; ++v4) {
-                    const float4 v = reinterpret_cast<const float4*>(xsum)[v4];
-                    X[4 * v4 + 0] = v.x;
-                    X[4 * v4 + 1] = v.y;
-                    X[4 * v4 + 2] = v.z;
-                    X[4 * v4 + 3] = v.w;
+        int si = team;
+        for (int tt = t0;; ++tt) {
+            // segment of tile tt inside [u0, u1): local stages up to b_end
+            const int b_end = ((tt + 1) * p.GP - u0 < nst) ? (tt + 1) * p.GP - u0 : nst;
+            for (; si < b_end; si += kTeams) {
+                const int slot = si % kStages;
+                const uint32_t jpar = (uint32_t)((si / kTeams) & 1);
+                Q4_TMTR(p, tr + 8 * (si / kTeams) + 0);
+                // group constants of this stage
+                float s0, r0, s1, r1;
+                uint32_t cc0, cc1;
+                group_constants(s_a, b_a, s0, r0, cc0);
+                group_constants(s_a >> 16, b_a >> 16, s1, r1, cc1);
+                s_a = s_b;
+                b_a = b_b;
+                s_b = s_c;
+                b_b = b_c;
+                load_sb(si + 3 * kTeams, s_c, b_c);
+                live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1),
+                                                                     8u, abort_flag));
+                Q4_TMTR(p, tr + 8 * (si / kTeams) + 1);
+                const uint8_t* sb = smem + slot * kStageBytes;
+                const uint8_t* nb = sb + row * 64;
+                const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
+                if (live) {
+                    uint32_t av[32];
+                    {
+                        const uint4 n0 = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
+                        const uint4 n1 = *reinterpret_cast<const uint4*>(nb + ((1 ^ sx) << 4));
+                        dequant64(n0, n1, cc0, av);
+                        tmem_st_32x32b_x32(aA, av);
+                    }
+                    tmem_wait_st();                    // av is reused next
+                    {
+                        const uint4 n2 = *reinterpret_cast<const uint4*>(nb + ((2 ^ sx) << 4));
+                        const uint4 n3 = *reinterpret_cast<const uint4*>(nb + ((3 ^ sx) << 4));
+                        dequant64(n2, n3, cc1, av);
+                        tmem_st_32x32b_x32(aA + 32u, av);
+                    }
+                    tmem_wait_st();
                 }
-            } else {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) X[m] = xsum[m];
-            }
-            if (MT == 1) {
-                acc[0] = __fmaf_rn(s, __uint_as_float(P[0]), __fmaf_rn(r, X[0], acc[0]));
-            } else {
-#pragma unroll
-                for (int m = 0; m + 1 < MT; m += 2) {
-                    fma2(acc[m], acc[m + 1], r, X[m], X[m + 1]);
-                    fma2(acc[m], acc[m + 1], s, __uint_as_float(P[m]), __uint_as_float(P[m + 1]));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ready[team]);
+                Q4_TMTR(p, tr + 8 * (si / kTeams) + 2);
+                live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], jpar, 4u, abort_flag));
+                if (live) {
+                    tc_fence_after();
+                    const float* xs0 = reinterpret_cast<const float*>(sb + kNibStage);
+                    const float* xs1 = reinterpret_cast<const float*>(sb + kNibStage + kRec);
+                    if (MT <= 8) {
+                        uint32_t P0[8], P1[8];
+                        tmem_ld_32x32b_x8(dP, P0);
+                        tmem_ld_32x32b_x8(dP + 16u, P1);
+                        tmem_wait_ld();
+                        fold_group<MT>(acc, P0, xs0, s0, r0);
+                        fold_group<MT>(acc, P1, xs1, s1, r1);
+                    } else {
+                        uint32_t P[16];
+                        tmem_ld_32x32b_x16(dP, P);
+                        tmem_wait_ld();
+                        fold_group<MT>(acc, P, xs0, s0, r0);
+                        tmem_ld_32x32b_x16(dP + 16u, P);
+                        tmem_wait_ld();
+                        fold_group<MT>(acc, P, xs1, s1, r1);
+                    }
                 }
+                // P and the slot (nibbles, records) have been read: the next MMAs of
+                // this team may overwrite P only after its next ready, the producer may refill
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                Q4_TMTR(p, tr + 8 * (si / kTeams) + 3);
             }
-        };
-        auto close_group = [&](int jj) {
-            const int uf = puS + jj, gf = 2 * pkst + jj;
-            if (uf >= u0 && uf < u1 && (uf == u1 - 1 || gf == p.G - 1)) {
-                const bool whole = gf == p.G - 1 && pt * p.G >= u0;
-                end_segment<MT>(p, acc, pt, whole, pt == t_first ? 0 : 1, cg, row, row, c_id, bcast, !*abort_flag);
-            }
-        };
-        // fold the previous stage: wait for its MMAs, read both groups' P, add s*P + r*X
-        auto fold_prev = [&]() {
-            const bool v0 = puS >= u0 && puS < u1, v1 = puS + 1 >= u0 && puS + 1 < u1;
-            const uint32_t par = (uint32_t)(((puS - 2 * S0) >> 1) & 1);
-            const bool w = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[cg], par, 4u, abort_flag));
-            const float* xs0 = reinterpret_cast<const float*>(smem + pslot * kStageBytes + kNibStage + 2048);
-            const float* xs1 = reinterpret_cast<const float*>(smem + pslot * kStageBytes + kNibStage + kRec + 2048);
-            if (w) {
-                tc_fence_after();
-                if (MT <= 8) {
-                    uint32_t P0[8], P1[8];
-                    tmem_ld_32x32b_x8(dP0, P0);
-                    tmem_ld_32x32b_x8(dP0 + 16u, P1);
-                    tmem_wait_ld();
-                    if (v0) fold_group(0, P0, xs0, ps0, pr0);
-                    close_group(0);
-                    if (v1) fold_group(1, P1, xs1, ps1, pr1);
-                } else {
-                    uint32_t P[32];
-                    tmem_ld_32x32b_x32(dP0, P);
-                    tmem_wait_ld();
-                    if (v0) fold_group(0, P, xs0, ps0, pr0);
-                    close_group(0);
-                    if (v1) fold_group(1, P + 16, xs1, ps1, pr1);
-                }
-            } else {
-                close_group(0);
-            }
-            close_group(1);
-        };
-
-        int slot = 0;
-        uint32_t ph = 0;
-        int kst = kS0, t = tS0;
-        int uS = 2 * S0;
-        // constants of the stage about to be dequantized, computed one iteration ahead
-        float cs0, cs1, cr0, cr1;
-        uint32_t cc0a, cc0b;
-        auto stage_constants = [&](int k) {
-            const int wsel = k & 3;
-            const uint32_t sw = wsel == 0 ? cur_s.x : wsel == 1 ? cur_s.y : wsel == 2 ? cur_s.z : cur_s.w;
-            const uint32_t bw = wsel == 0 ? cur_b.x : wsel == 1 ? cur_b.y : wsel == 2 ? cur_b.z : cur_b.w;
-            group_constants(sw, bw, cs0, cr0, cc0a);
-            group_constants(sw >> 16, bw >> 16, cs1, cr1, cc0b);
-        };
-        stage_constants(kst);
-        for (int si = 0; si < nst; ++si) {
-            Q4_TMTR(p, tr + 8 * si + 0);
-            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], ph, 8u, abort_flag));
-            Q4_TMTR(p, tr + 8 * si + 1);
-            const uint8_t* nb = smem + slot * kStageBytes + cg * kNibBox + row * 64;
-            const int sx = (row >> 1) & 3;
-            const uint32_t aA = aA0 + (uint32_t)((si & 1) * 64);
-            const bool g0 = live && uS >= u0, g1 = live && uS + 1 < u1;   // groups of the stage owned by this CTA
-            const uint4 n0 = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
-            const uint4 n1 = *reinterpret_cast<const uint4*>(nb + ((1 ^ sx) << 4));
-            const uint4 n2 = *reinterpret_cast<const uint4*>(nb + ((2 ^ sx) << 4));
-            const uint4 n3 = *reinterpret_cast<const uint4*>(nb + ((3 ^ sx) << 4));
-            if (g0) {
-                uint32_t a[32];
-                dequant64(n0, n1, cc0a, a);
-                tmem_st_32x32b_x32(aA, a);
-                tmem_wait_st();                        // the registers are reused next: store first
-            }
-            if (g1) {
-                uint32_t a[32];
-                dequant64(n2, n3, cc0b, a);
-                tmem_st_32x32b_x32(aA + 32u, a);
-                tmem_wait_st();
-            }
-            Q4_TMTR(p, tr + 8 * si + 2);
-            if (puS >= 0) fold_prev();
-            Q4_TMTR(p, tr + 8 * si + 3);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ready[cg]);
-            pslot = slot;
-            pkst = kst;
-            pt = t;
-            puS = uS;
-            ps0 = cs0;
-            ps1 = cs1;
-            pr0 = cr0;
-            pr1 = cr1;
-            if (++slot == kStages) {
-                slot = 0;
-                ph ^= 1u;
-            }
-            if (++kst == Gh) {
-                kst = 0;
-                ++t;
-            }
-            uS += 2;
-            if (si + 1 < nst) {
-                if ((kst & 3) == 0) {
-                    cur_s = nxt_s;
-                    cur_b = nxt_b;
-                    sb_next();
-                    if (S_sb < S0 + nst) load_sb(t_sb, k_sb, nxt_s, nxt_b);
-                }
-                stage_constants(kst);
-            }
+            // end of this CTA's segment of tile tt: all teams add their sums
+            const bool whole = u0 <= tt * p.GP && (tt + 1) * p.GP <= u1;
+            end_segment<MT>(p, acc, red, tt, whole, tt == t0 ? 0 : 1, team, row, c_id, bcast, !*abort_flag);
+            if (b_end >= nst) break;
         }
-        if (puS >= 0) fold_prev();
     }
 
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) {
         Q4_TMTR(p, 4001);
-        // the last CTA of the launch advances the epoch for the next launch's records
-        __threadfence();
-        const unsigned int prev = atomicAdd(p.finished, 1u);
-        if (prev == (unsigned int)p.C - 1u) {
-            *p.finished = 0u;
-            __threadfence();
-            atomicAdd(p.epoch, 1u);
-        }
+        Q4_TMGT(p, 2401 + 2 * c_id);
     }
     if (warp == 1) {
         tc_fence_after();
@@ -757,8 +682,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
 }
 
 inline int smem_bytes() { return kSmemBytes; }
-inline size_t partial_floats(int C) { return (size_t)C * 2 * kCG * 16 * kRowsCG; }
-inline size_t sem_ints(int C) { return (size_t)C * kCG; }
+inline size_t partial_floats(int C) { return (size_t)C * 2 * 16 * kRowsTile; }
+inline size_t sem_ints(int C) { return (size_t)C; }
 
 }  // namespace tm
 }  // namespace q4
