@@ -413,9 +413,9 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kRedBytes);   // nibbles and records landed
     uint64_t* empty = full + kStages;                  // slot free: the owning team has folded it
-    uint64_t* ready = empty + kStages;                 // [kTeams]: the team's A stored
-    uint64_t* done = ready + kTeams;                   // [kTeams]: the team's MMAs complete
-    uint64_t* fin = done + kTeams;                     // [kIssuers]
+    uint64_t* ready = empty + kStages;                 // [kTeams][2]: the team's A of one group stored
+    uint64_t* done = ready + 2 * kTeams;               // [kTeams][2]: the team's MMAs of one group complete
+    uint64_t* fin = done + 2 * kTeams;                 // [kIssuers]
     uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
     int* bcast = const_cast<int*>(abort_flag) + 1;
@@ -438,7 +438,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             mbar_init(&full[s], 2);
             mbar_init(&empty[s], 4);
         }
-        for (int i = 0; i < kTeams; ++i) {
+        for (int i = 0; i < 2 * kTeams; ++i) {
             mbar_init(&ready[i], 4);
             mbar_init(&done[i], 1);
         }
@@ -524,26 +524,30 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             const int slot = si % kStages;
             if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 2u, abort_flag)))
                 break;
-            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)((si / kTeams) & 1), 2u,
-                                                       abort_flag)))
-                break;
-            tc_fence_after();
             const uint64_t bd = bdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
             const uint32_t aS = tmem + (uint32_t)team * kColsTeam;
             const uint32_t dS = aS + kColP;
-            if (lane == 0) {
-                if (iss == 0) Q4_TMTR(p, 2000 + 2 * si);
+            bool ok = true;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
+            for (int g = 0; g < 2; ++g) {
+                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team * 2 + g], (uint32_t)((si / kTeams) & 1), 2u,
+                                                           abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    if (iss == 0 && g == 0) Q4_TMTR(p, 2000 + 2 * si);
                     const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_ts(dS + 16u * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
+                    tc_commit(&done[team * 2 + g]);
+                    if (iss == 0 && g == 1) Q4_TMTR(p, 2001 + 2 * si);
                 }
-                tc_commit(&done[team]);
-                if (iss == 0) Q4_TMTR(p, 2001 + 2 * si);
+                __syncwarp();
             }
-            __syncwarp();
+            if (!ok) break;
         }
         // no MMA of this warp may still run when tensor memory is freed
         if (lane == 0) {
@@ -577,11 +581,18 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                 bv = 0u;
             }
         };
-        // scale/bias words of this team's next three stages (prefetched)
-        uint32_t s_a, b_a, s_b, b_b, s_c, b_c;
-        load_sb(team, s_a, b_a);
-        load_sb(team + kTeams, s_b, b_b);
-        load_sb(team + 2 * kTeams, s_c, b_c);
+        // scale/bias words of this team's next stages (prefetched three stages ahead)
+        uint32_t s_b, b_b, s_c, b_c;
+        float s0, r0, s1, r1;                          // constants of the stage in hand
+        uint32_t cc0, cc1;
+        {
+            uint32_t s_a, b_a;
+            load_sb(team, s_a, b_a);
+            load_sb(team + kTeams, s_b, b_b);
+            load_sb(team + 2 * kTeams, s_c, b_c);
+            group_constants(s_a, b_a, s0, r0, cc0);
+            group_constants(s_a >> 16, b_a >> 16, s1, r1, cc1);
+        }
 
         float acc[MT];
 #pragma unroll
@@ -596,65 +607,62 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                 const int slot = si % kStages;
                 const uint32_t jpar = (uint32_t)((si / kTeams) & 1);
                 Q4_TMTR(p, tr + 8 * (si / kTeams) + 0);
-                // group constants of this stage
-                float s0, r0, s1, r1;
-                uint32_t cc0, cc1;
-                group_constants(s_a, b_a, s0, r0, cc0);
-                group_constants(s_a >> 16, b_a >> 16, s1, r1, cc1);
-                s_a = s_b;
-                b_a = b_b;
-                s_b = s_c;
-                b_b = b_c;
-                load_sb(si + 3 * kTeams, s_c, b_c);
                 live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1),
                                                                      8u, abort_flag));
                 Q4_TMTR(p, tr + 8 * (si / kTeams) + 1);
                 const uint8_t* sb = smem + slot * kStageBytes;
                 const uint8_t* nb = sb + row * 64;
                 const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
-                if (live) {
-                    uint32_t av[32];
-                    {
-                        const uint4 n0 = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
-                        const uint4 n1 = *reinterpret_cast<const uint4*>(nb + ((1 ^ sx) << 4));
-                        dequant64(n0, n1, cc0, av);
-                        tmem_st_32x32b_x32(aA, av);
+                // each group's A is handed over as soon as it is stored, so the MMAs of
+                // group 0 run while group 1 is dequantized
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    if (live) {
+                        uint32_t av[32];
+                        const uint4 na = *reinterpret_cast<const uint4*>(nb + (((2 * g) ^ sx) << 4));
+                        const uint4 nc = *reinterpret_cast<const uint4*>(nb + (((2 * g + 1) ^ sx) << 4));
+                        dequant64(na, nc, g == 0 ? cc0 : cc1, av);
+                        tmem_st_32x32b_x32(aA + 32u * g, av);
+                        tmem_wait_st();                // av is reused next
                     }
-                    tmem_wait_st();                    // av is reused next
-                    {
-                        const uint4 n2 = *reinterpret_cast<const uint4*>(nb + ((2 ^ sx) << 4));
-                        const uint4 n3 = *reinterpret_cast<const uint4*>(nb + ((3 ^ sx) << 4));
-                        dequant64(n2, n3, cc1, av);
-                        tmem_st_32x32b_x32(aA + 32u, av);
-                    }
-                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ready[team * 2 + g]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ready[team]);
                 Q4_TMTR(p, tr + 8 * (si / kTeams) + 2);
-                live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], jpar, 4u, abort_flag));
-                if (live) {
-                    tc_fence_after();
-                    const float* xs0 = reinterpret_cast<const float*>(sb + kNibStage);
-                    const float* xs1 = reinterpret_cast<const float*>(sb + kNibStage + kRec);
-                    if (MT <= 8) {
-                        uint32_t P0[8], P1[8];
-                        tmem_ld_32x32b_x8(dP, P0);
-                        tmem_ld_32x32b_x8(dP + 16u, P1);
-                        tmem_wait_ld();
-                        fold_group<MT>(acc, P0, xs0, s0, r0);
-                        fold_group<MT>(acc, P1, xs1, s1, r1);
-                    } else {
-                        uint32_t P[16];
-                        tmem_ld_32x32b_x16(dP, P);
-                        tmem_wait_ld();
-                        fold_group<MT>(acc, P, xs0, s0, r0);
-                        tmem_ld_32x32b_x16(dP + 16u, P);
-                        tmem_wait_ld();
-                        fold_group<MT>(acc, P, xs1, s1, r1);
+                // while the MMAs run: constants of this team's next stage
+                float ns0, nr0, ns1, nr1;
+                uint32_t ncc0, ncc1;
+                group_constants(s_b, b_b, ns0, nr0, ncc0);
+                group_constants(s_b >> 16, b_b >> 16, ns1, nr1, ncc1);
+                s_b = s_c;
+                b_b = b_c;
+                load_sb(si + 3 * kTeams, s_c, b_c);
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team * 2 + g], jpar, 4u, abort_flag));
+                    if (live) {
+                        tc_fence_after();
+                        const float* xs = reinterpret_cast<const float*>(sb + kNibStage + g * kRec);
+                        if (MT <= 8) {
+                            uint32_t P[8];
+                            tmem_ld_32x32b_x8(dP + 16u * g, P);
+                            tmem_wait_ld();
+                            fold_group<MT>(acc, P, xs, g == 0 ? s0 : s1, g == 0 ? r0 : r1);
+                        } else {
+                            uint32_t P[16];
+                            tmem_ld_32x32b_x16(dP + 16u * g, P);
+                            tmem_wait_ld();
+                            fold_group<MT>(acc, P, xs, g == 0 ? s0 : s1, g == 0 ? r0 : r1);
+                        }
                     }
                 }
+                s0 = ns0;
+                r0 = nr0;
+                cc0 = ncc0;
+                s1 = ns1;
+                r1 = nr1;
+                cc1 = ncc1;
                 // P and the slot (nibbles, records) have been read: the next MMAs of
                 // this team may overwrite P only after its next ready, the producer may refill
                 tc_fence_before();
