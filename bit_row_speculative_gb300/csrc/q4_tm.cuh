@@ -27,7 +27,7 @@
 //                order k0 k4 k1 k5 k2 k6 k3 k7 and scaled as above; rows >= M
 //                are zero.  A kernel for M <= 8 copies only the first 1088
 //                bytes (X and rows 0-7).
-//   q4_tm_kernel one persistent CTA per SM, 21 warps; tiles of 128 rows, a
+//   q4_tm_kernel one persistent CTA per SM, 16 warps; tiles of 128 rows, a
 //                stage is two groups (128 inputs) of one tile.
 //     warp 0       producer: per stage one 128-row x 64-byte nibble box (TMA,
 //                  64-byte swizzle) into a ring of kStages slots, and bulk
@@ -35,23 +35,24 @@
 //                  boxes of the first kStages stages are issued before the
 //                  kernel waits for its predecessor (they need nothing from
 //                  it); every record copy comes after that wait.
-//     warps 1..4   MMA issuers, one per team: per stage of the team 8 MMAs
+//     warps 1..3   MMA issuers, one per team: per stage of the team 8 MMAs
 //                  M128 N16 K16 (A = the dequantized weights in the team's
 //                  tensor memory, B = the x records in shared memory, D = the
 //                  team's P) and a commit to the team's "done" barrier.
-//     warps 5..20  four consumer teams of 4 warps; stage i belongs to team
-//                  i % 4, so each team has four stage periods for its own
-//                  chain of waits, tensor-memory stores and loads.  The ring
-//                  has a multiple of 4 slots, so a slot always serves the same
-//                  team, and each barrier is waited on by threads that pass
-//                  through its phases in order (a parity wait never sees a
-//                  phase two steps away).
-//                  Every team covers all 128 rows (one row per thread): it
-//                  dequantizes the stage's 2 x 64 nibbles of the row into A,
-//                  hands A over, waits for the MMAs, folds P into its own
-//                  fp32 sums with s, r and X, and frees the slot.  At the end
-//                  of each tile segment the four teams' sums are added in
-//                  team order through shared memory.
+//     warps 4..15  three consumer teams of 4 warps; stage i belongs to team
+//                  i % 3.  Every team covers all 128 rows (one row per
+//                  thread) and keeps two A buffers: in its iteration for stage
+//                  i it dequantizes stage i into one buffer while the MMAs of
+//                  its previous stage (i - 3) finish on the other, then folds
+//                  that previous stage's P into its own fp32 sums with s, r
+//                  and X, frees that stage's slot and hands stage i over.  So
+//                  the tensor core and the consumers overlap within a team,
+//                  and the three teams overlap with each other.  At the end of
+//                  each tile segment the teams' sums are added in team order
+//                  through shared memory.
+// The ring has a multiple of 3 slots, so a slot always serves the same team,
+// and every barrier is waited on by threads that pass through its phases in
+// order (a parity wait never sees a phase two steps away).
 // Work split: the T*G/2 (tile, group pair) units are cut into equal contiguous
 // ranges, one per CTA (stream-K).  A tile whose units span several CTAs is
 // finished by the last of them to arrive, which adds the partial sums in
@@ -72,15 +73,14 @@ namespace q4 {
 namespace tm {
 
 constexpr int kRowsTile = 128;              // rows per tile (tensor-memory lanes)
-constexpr int kTeams = 4;                   // consumer teams (one warpgroup each)
-// A multiple of kTeams: slot i % kStages then always belongs to team i % kTeams,
-// so every waiter on a slot's barriers has seen that slot's previous phase.
-constexpr int kStages = 12;
+constexpr int kTeams = 3;                   // consumer teams (one warpgroup each)
+constexpr int kStages = 15;                 // a multiple of kTeams
 static_assert(kStages % kTeams == 0, "each ring slot must belong to one team");
 constexpr int kIssuers = kTeams;            // one MMA issuer per team
-constexpr int kConsumerWarp0 = 1 + kIssuers;
-constexpr int kThreads = (kConsumerWarp0 + 4 * kTeams) * 32;   // 672
+constexpr int kConsumerWarp0 = 4;
+constexpr int kThreads = (kConsumerWarp0 + 4 * kTeams) * 32;   // 512
 constexpr int kConsumerThreads = kTeams * 128;
+static_assert(kIssuers + 1 <= kConsumerWarp0, "control warps");
 
 constexpr int kRec = 2112;                            // x record of one group
 constexpr int kRecHalf = 1088;                        // X and rows 0-7
@@ -90,10 +90,12 @@ constexpr int kStageBytes = ((kNibStage + 2 * kRec + 1023) / 1024) * 1024;
 constexpr int kRedBytes = kTeams * 16 * kRowsTile * 4;   // team sums of one segment
 constexpr int kBarrierBytes = 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + kRedBytes + kBarrierBytes + 1024 /* alignment slack */;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// tensor-memory columns per team: A (two groups x 32), P (two groups x 16)
-constexpr uint32_t kColsTeam = 96;
-constexpr uint32_t kColP = 64;
+// tensor-memory columns per team: A0, A1 (two groups x 32 each), P (two groups x 16)
+constexpr uint32_t kColsA = 64;
+constexpr uint32_t kColP = 2 * kColsA;
+constexpr uint32_t kColsTeam = kColP + 32;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kTeams * kColsTeam <= kTmemCols, "tensor memory over-subscribed");
 
@@ -292,7 +294,7 @@ __device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, 
     } else {
 #pragma unroll
         for (int m4 = 0; m4 < (MT + 3) / 4; ++m4) {
-            float X[4];
+            float X[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (MT >= 4) {
                 const float4 v = reinterpret_cast<const float4*>(xs)[m4];
                 X[0] = v.x;
@@ -304,23 +306,25 @@ __device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, 
                 X[1] = xs[1];
             }
 #pragma unroll
-            for (int i = 0; i < 4 && 4 * m4 + i + 1 < MT + 1; i += 2) {
+            for (int i = 0; i < 4; i += 2) {
                 const int m = 4 * m4 + i;
-                fma2(acc[m], acc[m + 1], r, X[i], X[i + 1]);
-                fma2(acc[m], acc[m + 1], s, __uint_as_float(P[m]), __uint_as_float(P[m + 1]));
+                if (m < MT) {
+                    fma2(acc[m], acc[m + 1], r, X[i], X[i + 1]);
+                    fma2(acc[m], acc[m + 1], s, __uint_as_float(P[m]), __uint_as_float(P[m + 1]));
+                }
             }
         }
     }
 }
 
-// End of a tile segment: the four teams' sums of rows [t*128, t*128+128) are
-// added in team order; a whole tile is stored, a partial one published and
-// finished by the last CTA to arrive (partials added in increasing CTA order).
-// Called by all 512 consumer threads; thread (team, row) handles m = team + 4j.
+// End of a tile segment: the teams' sums of rows [t*128, t*128+128) are added
+// in team order; a whole tile is stored, a partial one published and finished
+// by the last CTA to arrive (partials added in increasing CTA order).  Called
+// by all consumer threads; thread (team, row) handles m = team + kTeams*j.
 template <int MT>
 __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t, bool whole, int slot, int team,
                             int row, int c_id, int* bcast, bool live) {
-    constexpr int kJ = (MT + 3) / 4;
+    constexpr int kJ = (MT + kTeams - 1) / kTeams;
 #pragma unroll
     for (int m = 0; m < MT; ++m) red[(team * 16 + m) * kRowsTile + row] = acc[m];
     named_barrier(1, kConsumerThreads);
@@ -328,7 +332,7 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
     float v[kJ];
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
-        const int m = team + 4 * j;
+        const int m = team + kTeams * j;
         v[j] = 0.0f;
         if (m < MT) {
 #pragma unroll
@@ -339,7 +343,7 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
         if (live && n < p.N) {
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
-                const int m = team + 4 * j;
+                const int m = team + kTeams * j;
                 if (m < MT && m < p.M) p.y[(int64_t)m * p.N + n] = v[j];
             }
         }
@@ -348,7 +352,7 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
         if (live) {
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
-                const int m = team + 4 * j;
+                const int m = team + kTeams * j;
                 if (m < MT) __stcg(dst + m * kRowsTile, v[j]);
             }
         }
@@ -385,14 +389,14 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
                 const float* src = p.partials + (((int64_t)c * 2 + cslot) * 16) * kRowsTile + row;
 #pragma unroll
                 for (int j = 0; j < kJ; ++j) {
-                    const int m = team + 4 * j;
+                    const int m = team + kTeams * j;
                     if (m < MT) v[j] = __fadd_rn(v[j], __ldcg(src + m * kRowsTile));
                 }
             }
             if (n < p.N) {
 #pragma unroll
                 for (int j = 0; j < kJ; ++j) {
-                    const int m = team + 4 * j;
+                    const int m = team + kTeams * j;
                     if (m < MT && m < p.M) p.y[(int64_t)m * p.N + n] = v[j];
                 }
             }
@@ -413,9 +417,9 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kRedBytes);   // nibbles and records landed
     uint64_t* empty = full + kStages;                  // slot free: the owning team has folded it
-    uint64_t* ready = empty + kStages;                 // [kTeams][2]: the team's A of one group stored
-    uint64_t* done = ready + 2 * kTeams;               // [kTeams][2]: the team's MMAs of one group complete
-    uint64_t* fin = done + 2 * kTeams;                 // [kIssuers]
+    uint64_t* ready = empty + kStages;                 // [kTeams]: the team's A of a stage stored, its P free
+    uint64_t* done = ready + kTeams;                   // [kTeams]: the team's MMAs of a stage complete
+    uint64_t* fin = done + kTeams;                     // [kIssuers]
     uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
     int* bcast = const_cast<int*>(abort_flag) + 1;
@@ -438,7 +442,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             mbar_init(&full[s], 2);
             mbar_init(&empty[s], 4);
         }
-        for (int i = 0; i < 2 * kTeams; ++i) {
+        for (int i = 0; i < kTeams; ++i) {
             mbar_init(&ready[i], 4);
             mbar_init(&done[i], 1);
         }
@@ -515,54 +519,49 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         }
     } else if (warp <= kIssuers) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
-        const int iss = warp - 1;
+        const int team = warp - 1;
         const uint32_t idesc = idesc_bf16_f32(128, 16);
         // B: core matrices K-major, 128 B apart along K, rows 8-15 1024 B after rows 0-7
         const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(smem + kNibStage + kRecB), 128, 1024);
-        const int team = iss;
+        const uint32_t tbase = tmem + (uint32_t)team * kColsTeam;
         for (int si = team; si < nst; si += kTeams) {
             const int slot = si % kStages;
+            const int j = si / kTeams;
             if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 2u, abort_flag)))
                 break;
+            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)(j & 1), 2u, abort_flag))) break;
+            tc_fence_after();
             const uint64_t bd = bdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-            const uint32_t aS = tmem + (uint32_t)team * kColsTeam;
-            const uint32_t dS = aS + kColP;
-            bool ok = true;
+            const uint32_t aS = tbase + (uint32_t)(j & 1) * kColsA;
+            const uint32_t dS = tbase + kColP;
+            if (lane == 0) {
+                if (team == 0) Q4_TMTR(p, 2000 + 2 * si);
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team * 2 + g], (uint32_t)((si / kTeams) & 1), 2u,
-                                                           abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    if (iss == 0 && g == 0) Q4_TMTR(p, 2000 + 2 * si);
+                for (int g = 0; g < 2; ++g) {
                     const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_ts(dS + 16u * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
-                    tc_commit(&done[team * 2 + g]);
-                    if (iss == 0 && g == 1) Q4_TMTR(p, 2001 + 2 * si);
                 }
-                __syncwarp();
+                tc_commit(&done[team]);
+                if (team == 0) Q4_TMTR(p, 2001 + 2 * si);
             }
-            if (!ok) break;
+            __syncwarp();
         }
         // no MMA of this warp may still run when tensor memory is freed
         if (lane == 0) {
-            tc_commit(&fin[iss]);
-            mbar_wait(&fin[iss], 0, kWaitLimit);
+            tc_commit(&fin[team]);
+            mbar_wait(&fin[team], 0, kWaitLimit);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= kConsumerWarp0) {
         // ------------------------------------------------------------ consumer teams
-        const int team = (warp - kConsumerWarp0) >> 2;   // warps 5..8 team 0, ...; lane quarter = warp % 4
+        const int team = (warp - kConsumerWarp0) >> 2;
         const int q = warp & 3;                        // tensor-memory lane quarter of this warp
         const int row = q * 32 + lane;                 // row within the tile
         const uint32_t lane_field = (uint32_t)(q * 32) << 16;
-        const uint32_t aA = tmem + lane_field + (uint32_t)team * kColsTeam;
-        const uint32_t dP = aA + kColP;
+        const uint32_t tbase = tmem + lane_field + (uint32_t)team * kColsTeam;
+        const uint32_t dP = tbase + kColP;
         [[maybe_unused]] const int tr = (lane == 0 && q == 0 && team == 0) ? 1000 : 1 << 20;
 
         // scale and bias planes: this team's two groups of a stage are one 4-byte word per plane
@@ -583,7 +582,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         };
         // scale/bias words of this team's next stages (prefetched three stages ahead)
         uint32_t s_b, b_b, s_c, b_c;
-        float s0, r0, s1, r1;                          // constants of the stage in hand
+        float s0, r0, s1, r1;                          // constants of the stage being dequantized
         uint32_t cc0, cc1;
         {
             uint32_t s_a, b_a;
@@ -599,82 +598,95 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
         bool live = true;
 
-        int si = team;
-        for (int tt = t0;; ++tt) {
-            // segment of tile tt inside [u0, u1): local stages up to b_end
-            const int b_end = ((tt + 1) * p.GP - u0 < nst) ? (tt + 1) * p.GP - u0 : nst;
-            for (; si < b_end; si += kTeams) {
-                const int slot = si % kStages;
-                const uint32_t jpar = (uint32_t)((si / kTeams) & 1);
-                Q4_TMTR(p, tr + 8 * (si / kTeams) + 0);
-                live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1),
-                                                                     8u, abort_flag));
-                Q4_TMTR(p, tr + 8 * (si / kTeams) + 1);
-                const uint8_t* sb = smem + slot * kStageBytes;
-                const uint8_t* nb = sb + row * 64;
-                const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
-                // each group's A is handed over as soon as it is stored, so the MMAs of
-                // group 0 run while group 1 is dequantized
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    if (live) {
-                        uint32_t av[32];
-                        const uint4 na = *reinterpret_cast<const uint4*>(nb + (((2 * g) ^ sx) << 4));
-                        const uint4 nc = *reinterpret_cast<const uint4*>(nb + (((2 * g + 1) ^ sx) << 4));
-                        dequant64(na, nc, g == 0 ? cc0 : cc1, av);
-                        tmem_st_32x32b_x32(aA + 32u * g, av);
-                        tmem_wait_st();                // av is reused next
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ready[team * 2 + g]);
-                }
-                Q4_TMTR(p, tr + 8 * (si / kTeams) + 2);
-                // while the MMAs run: constants of this team's next stage
-                float ns0, nr0, ns1, nr1;
-                uint32_t ncc0, ncc1;
-                group_constants(s_b, b_b, ns0, nr0, ncc0);
-                group_constants(s_b >> 16, b_b >> 16, ns1, nr1, ncc1);
-                s_b = s_c;
-                b_b = b_c;
-                load_sb(si + 3 * kTeams, s_c, b_c);
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team * 2 + g], jpar, 4u, abort_flag));
-                    if (live) {
-                        tc_fence_after();
-                        const float* xs = reinterpret_cast<const float*>(sb + kNibStage + g * kRec);
-                        if (MT <= 8) {
-                            uint32_t P[8];
-                            tmem_ld_32x32b_x8(dP + 16u * g, P);
-                            tmem_wait_ld();
-                            fold_group<MT>(acc, P, xs, g == 0 ? s0 : s1, g == 0 ? r0 : r1);
-                        } else {
-                            uint32_t P[16];
-                            tmem_ld_32x32b_x16(dP + 16u * g, P);
-                            tmem_wait_ld();
-                            fold_group<MT>(acc, P, xs, g == 0 ? s0 : s1, g == 0 ? r0 : r1);
-                        }
-                    }
-                }
-                s0 = ns0;
-                r0 = nr0;
-                cc0 = ncc0;
-                s1 = ns1;
-                r1 = nr1;
-                cc1 = ncc1;
-                // P and the slot (nibbles, records) have been read: the next MMAs of
-                // this team may overwrite P only after its next ready, the producer may refill
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-                Q4_TMTR(p, tr + 8 * (si / kTeams) + 3);
+        // segments: tile t0 + k for k = 0 .. n_seg-1, each closed exactly once by every team
+        const int n_seg = (u1 - 1) / p.GP - t0 + 1;
+        int cur_seg = 0;
+        auto close_segments_before = [&](int seg) {
+            while (cur_seg < seg) {
+                const int tt = t0 + cur_seg;
+                const bool whole = u0 <= tt * p.GP && (tt + 1) * p.GP <= u1;
+                end_segment<MT>(p, acc, red, tt, whole, cur_seg == 0 ? 0 : 1, team, row, c_id, bcast,
+                                !*abort_flag);
+                ++cur_seg;
             }
-            // end of this CTA's segment of tile tt: all teams add their sums
-            const bool whole = u0 <= tt * p.GP && (tt + 1) * p.GP <= u1;
-            end_segment<MT>(p, acc, red, tt, whole, tt == t0 ? 0 : 1, team, row, c_id, bcast, !*abort_flag);
-            if (b_end >= nst) break;
+        };
+
+        // the stage handed over in the previous iteration, folded in this one
+        int pend = -1;
+        float ps0 = 0.f, pr0 = 0.f, ps1 = 0.f, pr1 = 0.f;
+        auto fold_pending = [&]() {
+            const int pslot = pend % kStages;
+            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], (uint32_t)((pend / kTeams) & 1), 4u,
+                                                                 abort_flag));
+            close_segments_before((u0 + pend) / p.GP - t0);
+            if (live) {
+                tc_fence_after();
+                const uint8_t* psb = smem + pslot * kStageBytes + kNibStage;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const float* xs = reinterpret_cast<const float*>(psb + g * kRec);
+                    if (MT <= 8) {
+                        uint32_t P[8];
+                        tmem_ld_32x32b_x8(dP + 16u * g, P);
+                        tmem_wait_ld();
+                        fold_group<MT>(acc, P, xs, g == 0 ? ps0 : ps1, g == 0 ? pr0 : pr1);
+                    } else {
+                        uint32_t P[16];
+                        tmem_ld_32x32b_x16(dP + 16u * g, P);
+                        tmem_wait_ld();
+                        fold_group<MT>(acc, P, xs, g == 0 ? ps0 : ps1, g == 0 ? pr0 : pr1);
+                    }
+                }
+            }
+            // that stage's slot (nibbles, records) has been read, and so has P
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[pslot]);
+        };
+
+        for (int si = team; si < nst; si += kTeams) {
+            const int slot = si % kStages;
+            const int j = si / kTeams;
+            Q4_TMTR(p, tr + 8 * j + 0);
+            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 8u,
+                                                                 abort_flag));
+            Q4_TMTR(p, tr + 8 * j + 1);
+            // dequantize into this stage's A buffer (the other one may still feed the previous MMAs)
+            if (live) {
+                const uint8_t* nb = smem + slot * kStageBytes + row * 64;
+                const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
+                const uint32_t aA = tbase + (uint32_t)(j & 1) * kColsA;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t av[32];
+                    const uint4 na = *reinterpret_cast<const uint4*>(nb + (((2 * g) ^ sx) << 4));
+                    const uint4 nc = *reinterpret_cast<const uint4*>(nb + (((2 * g + 1) ^ sx) << 4));
+                    dequant64(na, nc, g == 0 ? cc0 : cc1, av);
+                    tmem_st_32x32b_x32(aA + 32u * g, av);
+                    tmem_wait_st();                    // av is reused next
+                }
+            }
+            Q4_TMTR(p, tr + 8 * j + 2);
+            // fold the previous stage (its MMAs ran meanwhile); then P is free again
+            if (pend >= 0) fold_pending();
+            Q4_TMTR(p, tr + 8 * j + 3);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ready[team]);
+            // this stage becomes the pending one; constants of the team's next stage
+            pend = si;
+            ps0 = s0;
+            pr0 = r0;
+            ps1 = s1;
+            pr1 = r1;
+            group_constants(s_b, b_b, s0, r0, cc0);
+            group_constants(s_b >> 16, b_b >> 16, s1, r1, cc1);
+            s_b = s_c;
+            b_b = b_c;
+            load_sb(si + 3 * kTeams, s_c, b_c);
         }
+        if (pend >= 0) fold_pending();
+        close_segments_before(n_seg);
     }
 
     tc_fence_before();
