@@ -76,8 +76,9 @@ constexpr int kRowsTile = 128;              // rows per tile (tensor-memory lane
 constexpr int kTeams = 3;                   // consumer teams (one warpgroup each)
 constexpr int kStages = 15;                 // a multiple of kTeams
 static_assert(kStages % kTeams == 0, "each ring slot must belong to one team");
-constexpr int kIssuers = kTeams;            // one MMA issuer per team
-constexpr int kConsumerWarp0 = 4;
+constexpr int kIssuersPerTeam = 1;          // MMA issuing threads per team (they split the two groups)
+constexpr int kIssuers = kIssuersPerTeam * kTeams;
+constexpr int kConsumerWarp0 = 4;           // warps 4.. (warp % 4 = tensor-memory lane quarter)
 constexpr int kThreads = (kConsumerWarp0 + 4 * kTeams) * 32;   // 512
 constexpr int kConsumerThreads = kTeams * 128;
 static_assert(kIssuers + 1 <= kConsumerWarp0, "control warps");
@@ -444,7 +445,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         }
         for (int i = 0; i < kTeams; ++i) {
             mbar_init(&ready[i], 4);
-            mbar_init(&done[i], 1);
+            mbar_init(&done[i], kIssuersPerTeam);
         }
         for (int i = 0; i < kIssuers; ++i) mbar_init(&fin[i], 1);
         *abort_flag = 0;
@@ -519,7 +520,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         }
     } else if (warp <= kIssuers) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
-        const int team = warp - 1;
+        const int team = (warp - 1) / kIssuersPerTeam, gsel = (warp - 1) % kIssuersPerTeam;
         const uint32_t idesc = idesc_bf16_f32(128, 16);
         // B: core matrices K-major, 128 B apart along K, rows 8-15 1024 B after rows 0-7
         const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(smem + kNibStage + kRecB), 128, 1024);
@@ -535,23 +536,24 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             const uint32_t aS = tbase + (uint32_t)(j & 1) * kColsA;
             const uint32_t dS = tbase + kColP;
             if (lane == 0) {
-                if (team == 0) Q4_TMTR(p, 2000 + 2 * si);
+                if (team == 0 && gsel == 0) Q4_TMTR(p, 2000 + 2 * si);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
+                    if (g % kIssuersPerTeam != gsel) continue;
                     const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_ts(dS + 16u * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&done[team]);
-                if (team == 0) Q4_TMTR(p, 2001 + 2 * si);
+                if (team == 0 && gsel == 0) Q4_TMTR(p, 2001 + 2 * si);
             }
             __syncwarp();
         }
         // no MMA of this warp may still run when tensor memory is freed
         if (lane == 0) {
-            tc_commit(&fin[team]);
-            mbar_wait(&fin[team], 0, kWaitLimit);
+            tc_commit(&fin[warp - 1]);
+            mbar_wait(&fin[warp - 1], 0, kWaitLimit);
         }
         __syncwarp();
     } else if (warp >= kConsumerWarp0) {
@@ -567,31 +569,43 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         // scale and bias planes: this team's two groups of a stage are one 4-byte word per plane
         const uint8_t* splane = p.W + p.N * (p.K / 2);
         const uint8_t* bplane = splane + p.N * p.G * 2;
-        auto load_sb = [&](int si, uint32_t& sv, uint32_t& bv) {
-            const int u = u0 + si;
-            const int t = u / p.GP, gp = u - t * p.GP;
-            const int64_t n = (int64_t)t * kRowsTile + row;
-            if (si < nst && n < p.N) {
-                const int64_t off = (n * p.G + 2 * gp) * 2;
+        // cursor of the next scale/bias load: the team's stages in order, each
+        // kTeams units after the previous one (no divisions in the loop)
+        int ld_si = team, ld_t = (u0 + team) / p.GP, ld_gp = (u0 + team) - ld_t * p.GP;
+        auto load_next = [&](uint32_t& sv, uint32_t& bv) {
+            const int64_t n = (int64_t)ld_t * kRowsTile + row;
+            if (ld_si < nst && n < p.N) {
+                const int64_t off = (n * p.G + 2 * ld_gp) * 2;
                 sv = __ldg(reinterpret_cast<const uint32_t*>(splane + off));
                 bv = __ldg(reinterpret_cast<const uint32_t*>(bplane + off));
             } else {
                 sv = 0u;
                 bv = 0u;
             }
+            ld_si += kTeams;
+            ld_gp += kTeams;
+            while (ld_gp >= p.GP) {
+                ld_gp -= p.GP;
+                ++ld_t;
+            }
         };
-        // scale/bias words of this team's next stages (prefetched three stages ahead)
-        uint32_t s_b, b_b, s_c, b_c;
+        // Scale/bias words are loaded two team stages before their constants are
+        // formed, into two register pairs used alternately (the loop below is
+        // unrolled by two), so no instruction reads a register whose load is
+        // still in flight.
+        uint32_t sA, bA, sB, bB;
         float s0, r0, s1, r1;                          // constants of the stage being dequantized
         uint32_t cc0, cc1;
         {
             uint32_t s_a, b_a;
-            load_sb(team, s_a, b_a);
-            load_sb(team + kTeams, s_b, b_b);
-            load_sb(team + 2 * kTeams, s_c, b_c);
+            load_next(s_a, b_a);
+            load_next(sA, bA);
+            load_next(sB, bB);
             group_constants(s_a, b_a, s0, r0, cc0);
             group_constants(s_a >> 16, b_a >> 16, s1, r1, cc1);
         }
+        // tile of the team's current stage, advanced the same way
+        int st_t = (u0 + team) / p.GP, st_gp = (u0 + team) - st_t * p.GP;
 
         float acc[MT];
 #pragma unroll
@@ -612,30 +626,33 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         };
 
         // the stage handed over in the previous iteration, folded in this one
-        int pend = -1;
+        int pend = -1, pend_seg = 0;
         float ps0 = 0.f, pr0 = 0.f, ps1 = 0.f, pr1 = 0.f;
         auto fold_pending = [&]() {
             const int pslot = pend % kStages;
             live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], (uint32_t)((pend / kTeams) & 1), 4u,
                                                                  abort_flag));
-            close_segments_before((u0 + pend) / p.GP - t0);
+            Q4_TMTR(p, tr + 8 * (pend / kTeams) + 7);
+            close_segments_before(pend_seg);
             if (live) {
                 tc_fence_after();
                 const uint8_t* psb = smem + pslot * kStageBytes + kNibStage;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const float* xs = reinterpret_cast<const float*>(psb + g * kRec);
-                    if (MT <= 8) {
-                        uint32_t P[8];
-                        tmem_ld_32x32b_x8(dP + 16u * g, P);
-                        tmem_wait_ld();
-                        fold_group<MT>(acc, P, xs, g == 0 ? ps0 : ps1, g == 0 ? pr0 : pr1);
-                    } else {
-                        uint32_t P[16];
-                        tmem_ld_32x32b_x16(dP + 16u * g, P);
-                        tmem_wait_ld();
-                        fold_group<MT>(acc, P, xs, g == 0 ? ps0 : ps1, g == 0 ? pr0 : pr1);
-                    }
+                const float* xs0 = reinterpret_cast<const float*>(psb);
+                const float* xs1 = reinterpret_cast<const float*>(psb + kRec);
+                if (MT <= 8) {
+                    uint32_t P0[8], P1[8];
+                    tmem_ld_32x32b_x8(dP, P0);
+                    tmem_ld_32x32b_x8(dP + 16u, P1);
+                    tmem_wait_ld();
+                    fold_group<MT>(acc, P0, xs0, ps0, pr0);
+                    fold_group<MT>(acc, P1, xs1, ps1, pr1);
+                } else {
+                    uint32_t P0[16], P1[16];
+                    tmem_ld_32x32b_x16(dP, P0);
+                    tmem_ld_32x32b_x16(dP + 16u, P1);
+                    tmem_wait_ld();
+                    fold_group<MT>(acc, P0, xs0, ps0, pr0);
+                    fold_group<MT>(acc, P1, xs1, ps1, pr1);
                 }
             }
             // that stage's slot (nibbles, records) has been read, and so has P
@@ -644,7 +661,9 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             if (lane == 0) mbar_arrive(&empty[pslot]);
         };
 
-        for (int si = team; si < nst; si += kTeams) {
+        // one team stage: sw/bw hold the words of the team's next stage on entry
+        // and are reloaded with those of the stage after the one that follows
+        auto team_stage = [&](int si, uint32_t& sw, uint32_t& bw) {
             const int slot = si % kStages;
             const int j = si / kTeams;
             Q4_TMTR(p, tr + 8 * j + 0);
@@ -656,15 +675,20 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                 const uint8_t* nb = smem + slot * kStageBytes + row * 64;
                 const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
                 const uint32_t aA = tbase + (uint32_t)(j & 1) * kColsA;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t av[32];
-                    const uint4 na = *reinterpret_cast<const uint4*>(nb + (((2 * g) ^ sx) << 4));
-                    const uint4 nc = *reinterpret_cast<const uint4*>(nb + (((2 * g + 1) ^ sx) << 4));
-                    dequant64(na, nc, g == 0 ? cc0 : cc1, av);
-                    tmem_st_32x32b_x32(aA + 32u * g, av);
-                    tmem_wait_st();                    // av is reused next
+                uint32_t av0[32], av1[32];
+                {
+                    const uint4 na = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
+                    const uint4 nc = *reinterpret_cast<const uint4*>(nb + ((1 ^ sx) << 4));
+                    dequant64(na, nc, cc0, av0);
+                    tmem_st_32x32b_x32(aA, av0);
                 }
+                {
+                    const uint4 na = *reinterpret_cast<const uint4*>(nb + ((2 ^ sx) << 4));
+                    const uint4 nc = *reinterpret_cast<const uint4*>(nb + ((3 ^ sx) << 4));
+                    dequant64(na, nc, cc1, av1);
+                    tmem_st_32x32b_x32(aA + 32u, av1);
+                }
+                tmem_wait_st();
             }
             Q4_TMTR(p, tr + 8 * j + 2);
             // fold the previous stage (its MMAs ran meanwhile); then P is free again
@@ -673,17 +697,28 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ready[team]);
+            Q4_TMTR(p, tr + 8 * j + 4);
             // this stage becomes the pending one; constants of the team's next stage
             pend = si;
+            pend_seg = st_t - t0;
+            st_gp += kTeams;
+            while (st_gp >= p.GP) {
+                st_gp -= p.GP;
+                ++st_t;
+            }
             ps0 = s0;
             pr0 = r0;
             ps1 = s1;
             pr1 = r1;
-            group_constants(s_b, b_b, s0, r0, cc0);
-            group_constants(s_b >> 16, b_b >> 16, s1, r1, cc1);
-            s_b = s_c;
-            b_b = b_c;
-            load_sb(si + 3 * kTeams, s_c, b_c);
+            group_constants(sw, bw, s0, r0, cc0);
+            group_constants(sw >> 16, bw >> 16, s1, r1, cc1);
+            Q4_TMTR(p, tr + 8 * j + 5);
+            load_next(sw, bw);
+            Q4_TMTR(p, tr + 8 * j + 6);
+        };
+        for (int si = team; si < nst; si += 2 * kTeams) {
+            team_stage(si, sA, bA);
+            if (si + kTeams < nst) team_stage(si + kTeams, sB, bB);
         }
         if (pend >= 0) fold_pending();
         close_segments_before(n_seg);
