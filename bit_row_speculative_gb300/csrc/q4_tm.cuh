@@ -74,7 +74,7 @@ namespace tm {
 
 constexpr int kRowsTile = 128;              // rows per tile (tensor-memory lanes)
 constexpr int kTeams = 3;                   // consumer teams (one warpgroup each)
-constexpr int kStages = 15;                 // a multiple of kTeams
+constexpr int kStages = 12;                 // a multiple of kTeams
 static_assert(kStages % kTeams == 0, "each ring slot must belong to one team");
 constexpr int kIssuersPerTeam = 1;          // MMA issuing threads per team (they split the two groups)
 constexpr int kIssuers = kIssuersPerTeam * kTeams;
@@ -88,7 +88,7 @@ constexpr int kRecHalf = 1088;                        // X and rows 0-7
 constexpr int kRecB = 64;                             // offset of the core matrices in a record
 constexpr int kNibStage = kRowsTile * 64;             // 8 KB: 128 rows x 64 B (two groups)
 constexpr int kStageBytes = ((kNibStage + 2 * kRec + 1023) / 1024) * 1024;
-constexpr int kRedBytes = kTeams * 16 * kRowsTile * 4;   // team sums of one segment
+constexpr int kRedBytes = 2 * kTeams * 16 * kRowsTile * 4;   // team sums of a segment, two buffers
 constexpr int kBarrierBytes = 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + kRedBytes + kBarrierBytes + 1024 /* alignment slack */;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -325,6 +325,7 @@ __device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, 
 template <int MT>
 __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t, bool whole, int slot, int team,
                             int row, int c_id, int* bcast, bool live) {
+    // red: this segment's buffer (the caller alternates the two by segment)
     constexpr int kJ = (MT + kTeams - 1) / kTeams;
 #pragma unroll
     for (int m = 0; m < MT; ++m) red[(team * 16 + m) * kRowsTile + row] = acc[m];
@@ -357,11 +358,10 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
                 if (m < MT) __stcg(dst + m * kRowsTile, v[j]);
             }
         }
-        // every thread makes its own partial stores visible device-wide before
-        // the barrier, so thread 0's counter increment follows all of them; the
-        // last contributor fences again after the barrier that follows its
-        // increment before any thread reads the other CTAs' partials
-        __threadfence();
+        // the barrier orders every consumer thread's partial stores before
+        // thread 0's release (acq_rel) increment of the tile counter; the last
+        // contributor's acquire, followed by the next barrier, orders the other
+        // CTAs' partials before every thread's reads below
         named_barrier(1, kConsumerThreads);
         const int tu = t * p.GP;
         const int c_first = cta_of_unit(p.U, p.C, tu);
@@ -381,7 +381,6 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
         }
         named_barrier(1, kConsumerThreads);
         if (*bcast) {
-            __threadfence();
 #pragma unroll
             for (int j = 0; j < kJ; ++j) v[j] = 0.0f;
             for (int c = c_first; c <= c_last; ++c) {
@@ -403,8 +402,10 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
             }
         }
     }
-    // red (and bcast) are rewritten at the next segment end only after every thread passed here
-    named_barrier(1, kConsumerThreads);
+    // red alternates between two buffers by segment, so a buffer is rewritten
+    // only after every thread has passed the first barrier of the segment
+    // between (and with it finished reading here); bcast is written only on
+    // the partial path, between two barriers
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 }
@@ -462,7 +463,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     const uint32_t tmem = *tmem_base_slot;
     if (threadIdx.x == 0) {
         Q4_TMTR(p, 4000);
-        Q4_TMGT(p, 2400 + 2 * c_id);
+        Q4_TMGT(p, 2400 + 8 * c_id);
     }
 
     if (warp == 0) {
@@ -619,8 +620,15 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             while (cur_seg < seg) {
                 const int tt = t0 + cur_seg;
                 const bool whole = u0 <= tt * p.GP && (tt + 1) * p.GP <= u1;
-                end_segment<MT>(p, acc, red, tt, whole, cur_seg == 0 ? 0 : 1, team, row, c_id, bcast,
-                                !*abort_flag);
+                if (team == 0 && row == 0 && cur_seg < 2) Q4_TMGT(p, 2403 + 8 * c_id + 2 * cur_seg);
+                end_segment<MT>(p, acc, red + (cur_seg & 1) * (kTeams * 16 * kRowsTile), tt, whole,
+                                cur_seg == 0 ? 0 : 1, team, row, c_id, bcast, !*abort_flag);
+                if (team == 0 && row == 0 && cur_seg < 2) {
+                    Q4_TMGT(p, 2404 + 8 * c_id + 2 * cur_seg);
+#ifdef Q4_TRACE
+                    if (p.trace && !whole && *bcast) p.trace[2407 + 8 * c_id] |= 1ull << cur_seg;
+#endif
+                }
                 ++cur_seg;
             }
         };
@@ -667,6 +675,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             const int slot = si % kStages;
             const int j = si / kTeams;
             Q4_TMTR(p, tr + 8 * j + 0);
+            if (si == 0 && row == 0) Q4_TMGT(p, 2402 + 8 * c_id);
             live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 8u,
                                                                  abort_flag));
             Q4_TMTR(p, tr + 8 * j + 1);
@@ -728,7 +737,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     __syncthreads();
     if (threadIdx.x == 0) {
         Q4_TMTR(p, 4001);
-        Q4_TMGT(p, 2401 + 2 * c_id);
+        Q4_TMGT(p, 2401 + 8 * c_id);
     }
     if (warp == 1) {
         tc_fence_after();
