@@ -1,4 +1,5 @@
-// Production Q4 verify-matmul kernel for sm_103a (K a multiple of 512).
+// Two-launch tensor-memory Q4 verify-matmul kernel for sm_103a (K a multiple
+// of 512), used by q4_matmul_noalloc on its fixed scratch array.
 //
 // y[m,n] = sum_g ( s[n,g] * P[m,n,g] + r[n,g] * X[m,g] )
 //   P[m,n,g] = sum_{k in g} (q[n,k] - c[n,g]) * x[m,k]      (tensor core, exact products)
