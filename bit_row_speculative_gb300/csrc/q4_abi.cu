@@ -417,9 +417,25 @@ q4_status check_glue_args(const float* y, int M, int64_t n_prev, int64_t K, int 
     return Q4_OK;
 }
 
+// One cluster of glue::slices(K) CTAs per row, chained by programmatic dependent launch.
 q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind, void* x, cudaStream_t stream) {
-    cudaError_t e = launch_pdl(q4::glue::glue_kernel, dim3((unsigned)M), dim3(q4::glue::kThreads), 0, stream, y, n_prev,
-                               K, kind, kGlueEps, static_cast<uint16_t*>(x));
+    const int S = q4::glue::slices(K);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S, (unsigned)M);
+    cfg.blockDim = dim3(q4::glue::kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, q4::glue::glue_kernel, y, n_prev, K, kind, kGlueEps,
+                                       static_cast<uint16_t*>(x));
     if (e != cudaSuccess) return cuda_fail(e, "launching the glue kernel");
     return Q4_OK;
 }

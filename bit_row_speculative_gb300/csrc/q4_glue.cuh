@@ -7,31 +7,47 @@
 //
 // The pages' own between-layer operators (attention, Gated DeltaNet, gated
 // norms) are not on the matmul path; this fixed, bounded stand-in keeps the
-// values of a long chain of linears in range.  One CTA per row.
+// values of a long chain of linears in range.
+//
+// Work split: one thread-block cluster per row, S = slices(K) CTAs (at most 8)
+// each owning a contiguous slice of the row, so a step's glue runs on up to
+// 8*M SMs instead of M.  S depends on K only.
 //
 // Arithmetic: the definition is evaluated as if in double, at single-precision
 // cost.  The sum of squares is kept as an unevaluated pair of floats (each
 // square split exactly by an fma, the pairs added with error-free two-sums),
-// which carries about 48 significant bits; its per-thread pairs are combined
-// in a fixed tree, and the scale 1/sqrt(ss/K + eps) is formed in double.  Each
-// output is first computed in float; only when that value lies within a few
-// float ulps of a bf16 rounding boundary -- where float error could decide
-// the rounding -- is the element recomputed entirely in double (exp included)
-// and rounded from there.  Each row's result depends on that row alone.
+// which carries about 48 significant bits.  Each CTA reduces its slice in a
+// fixed order (thread-strided partials, then a fixed tree over lanes and
+// warps); the slices are then combined in cluster-rank order through
+// distributed shared memory, and the scale 1/sqrt(ss/K + eps) is formed in
+// double.  Each output is first computed in float; only when that value lies
+// within a few float ulps of a bf16 rounding boundary -- where float error
+// could decide the rounding -- is the element recomputed entirely in double
+// (exp included) and rounded from there.  Each row's result depends on that
+// row and K alone.
 // Programmatic dependent launch: the kernel lets the next kernel start at once
-// and reads y only after the preceding kernel finished.
+// and reads y only after the preceding kernel finished.  The cluster barrier is
+// a hardware barrier among CTAs that are always co-scheduled.
 #pragma once
 
 #include <cstdint>
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 namespace q4 {
 namespace glue {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;
+constexpr int kMaxSlices = 8;                 // portable cluster size
+constexpr int64_t kSliceMin = 1024;           // inputs per slice below which fewer slices are used
 // An output computed in float is trusted unless its low 16 bits (the bits
 // bf16 rounding drops) are within this many float ulps of the halfway point.
 constexpr int kTieMargin = 16;
+
+inline int slices(int64_t K) {
+    int64_t s = (K + kSliceMin - 1) / kSliceMin;
+    return (int)(s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s));
+}
 
 __device__ __forceinline__ float value_f(const float* yr, int64_t K, int64_t k, int kind) {
     const float a = yr[k];
@@ -54,16 +70,37 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float p, float e) {
     lo = __fadd_rn(lo, __fadd_rn(err, e));
 }
 
+// grid (S, M), cluster (S, 1, 1): CTA (s, m) owns inputs [s*L, min(K, (s+1)*L)) of row m.
 __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict__ y, int64_t n_prev, int64_t K,
                                                         int kind, double eps, uint16_t* __restrict__ x) {
+    namespace cg = cooperative_groups;
     __shared__ float part_hi[kThreads / 32], part_lo[kThreads / 32];
-    __shared__ double inv_s;
+    __shared__ float slice_sum[2];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");     // y comes from the preceding kernel
-    const int m = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = (int)gridDim.x;
+    const int s = (int)blockIdx.x;
+    const int m = (int)blockIdx.y;
+    const int64_t L = (K + S - 1) / S;
+    const int64_t k0 = (int64_t)s * L;
+    const int64_t k1 = (k0 + L < K) ? k0 + L : K;
     const float* yr = y + (int64_t)m * n_prev;
+
     float hi = 0.0f, lo = 0.0f;
-    for (int64_t k = threadIdx.x; k < K; k += kThreads) {
+    int64_t k = k0 + threadIdx.x;
+    // four independent loads in flight per thread, then the squares in increasing k
+    for (; k + 3 * kThreads < k1; k += 4 * kThreads) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = value_f(yr, K, k + u * kThreads, kind);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float p = __fmul_rn(v[u], v[u]);
+            ff_add(hi, lo, p, __fmaf_rn(v[u], v[u], -p));
+        }
+    }
+    for (; k < k1; k += kThreads) {
         const float v = value_f(yr, K, k, kind);
         const float p = __fmul_rn(v, v);
         ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
@@ -79,28 +116,35 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         part_lo[threadIdx.x >> 5] = lo;
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-        float th = part_hi[threadIdx.x], tl = part_lo[threadIdx.x];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float oh = __shfl_xor_sync(0xFFFFFFFFu, th, o), ol = __shfl_xor_sync(0xFFFFFFFFu, tl, o);
-            ff_add(th, tl, oh, ol);
-        }
-        if (threadIdx.x == 0) inv_s = 1.0 / sqrt(((double)th + (double)tl) / (double)K + eps);
+    if (threadIdx.x == 0) {
+        float th = part_hi[0], tl = part_lo[0];
+        for (int w = 1; w < kThreads / 32; ++w) ff_add(th, tl, part_hi[w], part_lo[w]);
+        slice_sum[0] = th;
+        slice_sum[1] = tl;
     }
-    __syncthreads();
+    cluster.sync();                                   // every slice's sum is in its CTA's shared memory
+    __shared__ double inv_s;
+    if (threadIdx.x == 0) {
+        float th = 0.0f, tl = 0.0f;
+        for (int r = 0; r < S; ++r) {                 // slices in rank order
+            const float* other = cluster.map_shared_rank(slice_sum, r);
+            ff_add(th, tl, other[0], other[1]);
+        }
+        inv_s = 1.0 / sqrt(((double)th + (double)tl) / (double)K + eps);
+    }
+    cluster.sync();                                   // no CTA leaves while another still reads its sum
     const double inv = inv_s;
     const float inv_f = (float)inv;
     uint16_t* xr = x + (int64_t)m * K;
-    for (int64_t k = threadIdx.x; k < K; k += kThreads) {
-        const float t = __fmul_rn(value_f(yr, K, k, kind), inv_f);
+    for (int64_t kk = k0 + threadIdx.x; kk < k1; kk += kThreads) {
+        const float t = __fmul_rn(value_f(yr, K, kk, kind), inv_f);
         const int low = (int)(__float_as_uint(t) & 0xFFFFu);
         __nv_bfloat16 h;
         if (abs(low - 0x8000) <= kTieMargin)
-            h = __double2bfloat16(value_d(yr, K, k, kind) * inv);    // near a tie: decide in double
+            h = __double2bfloat16(value_d(yr, K, kk, kind) * inv);   // near a tie: decide in double
         else
             h = __float2bfloat16_rn(t);
-        xr[k] = *reinterpret_cast<const uint16_t*>(&h);
+        xr[kk] = *reinterpret_cast<const uint16_t*>(&h);
     }
 }
 
