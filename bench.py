@@ -345,6 +345,32 @@ def run_ours(args, rank, world, local_rank):
     if args.workload == "attn_sweep":
         ratio = per_m["attn_in_M16"]["us_per_call"] / per_m["attn_in_M1"]["us_per_call"]
 
+    # LM head: the sampling epilogue (top-32, temperature 1, top_p 0.95) on the
+    # head's own logits; bytes = the logits read once + the 32 (index, prob) pairs per row
+    epilogue = None
+    if args.workload == "lm_head":
+        label, N, K, Ms = spec[0]
+        yl = ys[(label, Ms[0])]
+        ei = torch.empty((yl.shape[0], 32), dtype=torch.int32, device=dev)
+        ep = torch.empty((yl.shape[0], 32), dtype=torch.float32, device=dev)
+        reps = 50
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                q4.topk_probs(yl, 32, 1.0, 0.95, idx=ei, probs=ep, stream=stream)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(reps):
+                q4.topk_probs(yl, 32, 1.0, 0.95, idx=ei, probs=ep, stream=stream)
+            a1.record(stream)
+        stream.synchronize()
+        q4.device_status(stream)
+        us = a0.elapsed_time(a1) / reps * 1e3
+        ebytes = yl.numel() * 4 + yl.shape[0] * 32 * 8
+        epilogue = {"what": "q4_topk_probs top_k=32 T=1 top_p=0.95 on the head's logits", "M": yl.shape[0],
+                    "us_per_call": round(us, 3), "GBs": round(ebytes / (us * 1e-6) / 1e9, 1),
+                    "launches_per_call": 2}
+
     # end to end through the public API with host buffers: per call, pinned
     # host x -> device, the matmul, device y -> pinned host
     e2e = None
@@ -391,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
                          f"({l2 / 2**20:.0f} MiB); one CUDA graph per M",
                    "parallelism": f"replicas x{world}"},
         "per_M": per_m, "ratio_M16_over_M1": None if ratio is None else round(ratio, 4),
+        "sampling_epilogue": epilogue,
         "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,

@@ -29,7 +29,7 @@ GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).
 SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_glue", "q4_decode_step_workspace_bytes",
-           "q4_decode_step", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
+           "q4_decode_step", "q4_topk_probs", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
 
 GLUE_NONE = 0
 GLUE_RMSNORM = 1
@@ -66,6 +66,9 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.q4_decode_step.restype = c.c_int
     lib.q4_decode_step.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p,
                                    c.c_void_p]
+    lib.q4_topk_probs.restype = c.c_int
+    lib.q4_topk_probs.argtypes = [c.c_void_p, c.c_int, c.c_int64, c.c_int, c.c_float, c.c_float, c.c_void_p,
+                                  c.c_void_p, c.c_void_p]
     lib.q4_check_wait_timeout.restype = c.c_int
     lib.q4_check_wait_timeout.argtypes = [c.c_longlong, c.c_void_p]
     lib.q4_device_status.restype = c.c_int
@@ -201,6 +204,19 @@ def decode_step(layers, x0, y_last=None, workspace=None, stream=None):
 def matmul_raw(x_ptr: int, W_ptr: int, M: int, N: int, K: int, y_ptr: int, stream_handle: int) -> None:
     """Pointer-level call of q4_matmul (for callers that manage their own buffers)."""
     _check(lib().q4_matmul(x_ptr, W_ptr, M, N, K, y_ptr, stream_handle))
+
+
+def topk_probs(logits, top_k: int, temperature: float, top_p: float, idx=None, probs=None, stream=None):
+    """Sampling epilogue: (idx int32 [M, 32], probs fp32 [M, 32]) of fp32 device logits [M, N]."""
+    import torch
+    M, N = logits.shape
+    if idx is None:
+        idx = torch.empty((M, 32), dtype=torch.int32, device=logits.device)
+    if probs is None:
+        probs = torch.empty((M, 32), dtype=torch.float32, device=logits.device)
+    _check(lib().q4_topk_probs(logits.data_ptr(), M, N, int(top_k), float(temperature), float(top_p),
+                               idx.data_ptr(), probs.data_ptr(), _stream_handle(stream)))
+    return idx, probs
 
 
 def check_wait_timeout(limit_cycles: int, stream=None) -> None:

@@ -160,6 +160,23 @@ size_t q4_decode_step_workspace_bytes(const q4_layer* layers, int n_layers, int 
 q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, int M, void* workspace,
                          size_t workspace_bytes, float* y_last, q4_stream_t stream);
 
+/* Sampling epilogue of the LM head ("Splash engine" analysis, section "Exact,
+ * up to top-32": the target's probabilities are the temperature softmax over
+ * its first top_k entries, truncated by top_p, renormalized; top_k <= 32).
+ *   logits : device, fp32 [M, N] row-major (e.g. the y of the LM-head matmul).
+ *   M : 1..16.  N : top_k .. 1,048,576.  top_k : 1..32.  temperature > 0.
+ *   top_p > 0 (>= 1 keeps all top_k entries).
+ *   idx   : device, int32 [M, 32]: the top_k entries of each row by logit,
+ *           largest first, equal logits by lower index first (so the result is
+ *           unique); -1 past top_k.
+ *   probs : device, fp32 [M, 32]: p_j = exp((l_j - l_0)/T) / sum over the
+ *           top_k; the shortest prefix whose cumulative probability reaches
+ *           top_p is kept and renormalized; 0 for the rest.  Computed in double.
+ * All pointers 16-byte aligned.  Asynchronous on `stream`; uses the library's
+ * per-device scratch (the same ordering rules as q4_matmul). */
+q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float temperature, float top_p,
+                        int32_t* idx, float* probs, q4_stream_t stream);
+
 /* Self-check of the timeout reporting path.  Launches one thread on `stream`
  * that waits, with the same bounded wait every kernel of this library uses, on
  * a barrier that nothing signals; after `limit_cycles` SM clock cycles

@@ -130,3 +130,21 @@ def test_wait_check_rejects_bad_limits(limit):
     lib = q4.lib()
     assert lib.q4_check_wait_timeout(limit, None) == q4.Q4_ERR_INVALID_ARG
     assert "limit_cycles" in lib.q4_last_error().decode()
+
+
+@pytest.mark.parametrize("M,N,k,T,p,align,status", [
+    (0, 100, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (17, 100, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, 100, 0, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, 100, 33, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, 5, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, 100, 8, 0.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, 100, 8, float("nan"), 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, 100, 8, 1.0, 0.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (2, (1 << 20) + 1, 8, 1.0, 1.0, 0, q4.Q4_ERR_UNSUPPORTED_SHAPE),
+    (2, 100, 8, 1.0, 1.0, 4, q4.Q4_ERR_MISALIGNED),
+])
+def test_topk_rejects_bad_arguments(M, N, k, T, p, align, status):
+    lib = q4.lib()
+    rc = lib.q4_topk_probs(16 + align, M, N, k, T, p, 16, 16, None)
+    assert rc == status, (rc, lib.q4_last_error())

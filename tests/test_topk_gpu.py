@@ -1,0 +1,89 @@
+"""q4_topk_probs on the GPU against the oracle (oracle/topk.py): indices bit-exact
+(the order logit-descending, ties to the lower index, is unique), probabilities
+within 2 float ulps of the double-precision oracle.  LM-head-sized rows
+(248,320 logits) with planted ties across slice boundaries, every M, several
+top_k / temperature / top_p, rows independent of the other rows, determinism,
+and the epilogue chained after the LM-head matmul."""
+import numpy as np
+import pytest
+import torch
+
+import bit_row_speculative_gb300 as q4
+import synth_inputs as si
+from oracle import topk as T
+
+pytestmark = pytest.mark.gpu
+
+VOCAB = 248320
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def _logits(M, N, seed, ties=True):
+    g = torch.Generator().manual_seed(seed)
+    y = (torch.randn((M, N), generator=g) * 3.0).to(torch.float32)
+    if ties:
+        # the row's maximum copied to other positions, some across 16K-slice boundaries
+        for m in range(M):
+            j = int(torch.argmax(y[m]))
+            for t in (5, 16383, 16384, 70000, N - 1):
+                if t < N:
+                    y[m, t] = y[m, j]
+            y[m, 3] = y[m, 16390] = -0.0
+            y[m, 4] = 0.0
+    return y
+
+
+def _check(y, k, temp, p):
+    idx, pr = q4.topk_probs(y.cuda(), k, temp, p)
+    q4.device_status()
+    ref_i, ref_p = T.topk_probs(y.numpy(), k, temp, p)
+    assert np.array_equal(idx.cpu().numpy(), ref_i), "indices differ from the oracle"
+    got = pr.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref_p) <= 2.0 * np.spacing(np.float32(np.maximum(ref_p, 1e-38))) + 1e-45)
+
+
+@pytest.mark.parametrize("M", [1, 3, 16])
+@pytest.mark.parametrize("k,temp,p", [(32, 1.0, 1.0), (20, 0.7, 0.95), (1, 1.0, 1.0), (8, 2.5, 0.5)])
+def test_lm_head_rows_against_oracle(M, k, temp, p):
+    _check(_logits(M, VOCAB, 100 + M + k), k, temp, p)
+
+
+@pytest.mark.parametrize("N", [32, 100, 16384, 16385, 40000])
+def test_small_and_ragged_rows(N):
+    _check(_logits(4, N, N, ties=N > 20000), 32 if N >= 32 else N, 1.3, 0.9)
+
+
+def test_all_equal_logits():
+    y = torch.full((2, 50000), 1.25, dtype=torch.float32)
+    idx, pr = q4.topk_probs(y.cuda(), 32, 1.0, 1.0)
+    assert idx.cpu()[0].tolist() == list(range(32))
+    assert torch.all(pr.cpu() == 1.0 / 32)
+
+
+def test_rows_independent_and_deterministic():
+    y = _logits(16, VOCAB, 7)
+    idx, pr = q4.topk_probs(y.cuda(), 32, 0.8, 0.9)
+    for m in (0, 9, 15):
+        i1, p1 = q4.topk_probs(y[m:m + 1].contiguous().cuda(), 32, 0.8, 0.9)
+        assert torch.equal(i1[0].cpu(), idx[m].cpu()) and torch.equal(p1[0].cpu(), pr[m].cpu())
+    i2, p2 = q4.topk_probs(y.cuda(), 32, 0.8, 0.9)
+    assert torch.equal(i2, idx) and torch.equal(p2, pr)
+
+
+def test_after_lm_head_matmul():
+    """The epilogue on the LM head's own output, chained on one stream."""
+    N, K = si.SHAPES["lm_head"]
+    W = si.make_weights(N, K, si.w_seed(4), device="cuda")
+    x = si.make_x(16, K, si.x_seed(4), device="cuda")
+    y = q4.matmul(x, W, N, K)
+    idx, pr = q4.topk_probs(y, 32, 1.0, 0.95)
+    q4.device_status()
+    ref_i, ref_p = T.topk_probs(y.cpu().numpy(), 32, 1.0, 0.95)
+    assert np.array_equal(idx.cpu().numpy(), ref_i)
+    assert np.allclose(pr.cpu().numpy(), ref_p, rtol=3e-7, atol=1e-30)
