@@ -68,7 +68,8 @@ struct DeviceInfo {
     float* partials = nullptr;      // split-K partial sums of the tensor-core kernel
     int* sems = nullptr;            // per-tile arrival counters (zero between launches)
     uint8_t* xt = nullptr;          // prepared x records (one per group of 64 inputs)
-    uint64_t* topk_cand = nullptr;  // sampling epilogue: per-slice candidates [16][64][32]
+    uint64_t* topk_cand = nullptr;  // sampling epilogue: per-slice candidates [16][128][32]
+    int* topk_tickets = nullptr;    // sampling epilogue: per-row arrival counters (zero between launches)
     unsigned int* error_word = nullptr;
 };
 
@@ -148,9 +149,6 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_tm<4>();
             if (a == cudaSuccess) a = prepare_tm<8>();
             if (a == cudaSuccess) a = prepare_tm<16>();
-            if (a == cudaSuccess)
-                a = cudaFuncSetAttribute(q4::topk::topk_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)q4::topk::slice_smem_bytes());
             if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
             if (!g_encode) {
                 void* fn = nullptr;
@@ -172,6 +170,8 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * q4::prep::kRecordBytes);
             if (a == cudaSuccess)
                 a = cudaMalloc(&d.topk_cand, (size_t)Q4_MAX_ROWS * q4::topk::kMaxSlices * q4::topk::kWidth * sizeof(uint64_t));
+            if (a == cudaSuccess) a = cudaMalloc(&d.topk_tickets, (size_t)Q4_MAX_ROWS * sizeof(int));
+            if (a == cudaSuccess) a = cudaMemset(d.topk_tickets, 0, (size_t)Q4_MAX_ROWS * sizeof(int));
             if (a == cudaSuccess) a = cudaMemset(d.sems, 0, sbytes);
             if (a == cudaSuccess) a = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), q4_device_error_word);
             if (a == cudaSuccess) a = cudaDeviceSynchronize();
@@ -712,9 +712,8 @@ q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float 
     if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
     if (top_k < 1 || top_k > kWidth) return fail(Q4_ERR_INVALID_ARG, "top_k = %d is outside 1..%d", top_k, kWidth);
     if (N < top_k) return fail(Q4_ERR_INVALID_ARG, "N = %lld is smaller than top_k = %d", (long long)N, top_k);
-    if (N > (int64_t)kMaxSlice * kMaxSlices)
-        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "N = %lld exceeds %lld", (long long)N,
-                    (long long)kMaxSlice * kMaxSlices);
+    if (N > (int64_t)kSlice * kMaxSlices)
+        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "N = %lld exceeds %lld", (long long)N, (long long)kSlice * kMaxSlices);
     if (!(temperature > 0.0f) || !(temperature < 3.0e38f))
         return fail(Q4_ERR_INVALID_ARG, "temperature must be positive and finite");
     if (!(top_p > 0.0f)) return fail(Q4_ERR_INVALID_ARG, "top_p must be positive");
@@ -725,14 +724,11 @@ q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float 
     q4_status s = device_setup(&dev, &info);
     if (s != Q4_OK) return s;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int S = (int)((N + kMaxSlice - 1) / kMaxSlice);
-    const int64_t L = (N + S - 1) / S;
-    cudaError_t e = launch_pdl(topk_slice_kernel, dim3((unsigned)S, (unsigned)M), dim3(kSliceThreads),
-                               slice_smem_bytes(), st, logits, N, L, info->topk_cand);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the top-k slice kernel");
-    e = launch_pdl(topk_merge_kernel, dim3((unsigned)M), dim3(kMergeThreads), 0, st,
-                   static_cast<const uint64_t*>(info->topk_cand), S, top_k, temperature, top_p, idx, probs);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the top-k merge kernel");
+    const int S = (int)((N + kSlice - 1) / kSlice);
+    const int64_t L = ((N + S - 1) / S + 3) / 4 * 4;          // <= kSlice; slices start 16-byte aligned when N % 4 == 0
+    const cudaError_t e = launch_pdl(topk_kernel, dim3((unsigned)S, (unsigned)M), dim3(kThreads), 0, st, logits, N, L,
+                                     top_k, temperature, top_p, info->topk_cand, info->topk_tickets, idx, probs);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the top-k kernel");
     return Q4_OK;
 }
 

@@ -4,25 +4,35 @@
 // section "Exact, up to top-32").
 //
 // Order: logit descending, equal logits by lower index first, so the selected
-// set and its order are unique.  Logits are compared through a monotone 32-bit
-// key (sign-magnitude flipped; -0 counted as +0); NaN logits are outside the
-// contract.
+// set and its order are unique.  Each logit becomes a 64-bit candidate
+// (monotone 32-bit key of the float << 32 | ~index): a larger candidate ranks
+// first, and no two candidates are equal.  -0 counts as +0; NaN logits are
+// outside the contract.
 //
-// Phase 1 (topk_slice_kernel, grid (S, M)): CTA (s, m) stages slice s of row m
-// (at most kMaxSlice logits) in shared memory, finds its 32nd largest key by an
-// exact 8-bit radix select (4 rounds of histograms, MSB first), and writes its
-// top min(32, slice length) entries -- every key above that threshold, then
-// the lowest-index keys equal to it -- as 64-bit candidates (key << 32 | ~index,
-// so a larger candidate ranks first) in index order.  The global top 32 of a row
-// is contained in the union of its slices' top 32.
-// Phase 2 (topk_merge_kernel, grid M): sorts a row's S*32 candidates (bitonic,
-// descending) and one thread forms the probabilities in double in rank order:
-// p_j = exp((l_j - l_0)/T) / sum_i exp((l_i - l_0)/T) over the top_k, keeps the
-// shortest prefix whose cumulative probability reaches top_p (all if
-// top_p >= 1), renormalizes it, and stores fp32 probabilities and int32
-// indices (-1 past top_k, probability 0 past the kept prefix).
-// Both kernels use programmatic dependent launch and read the logits only
-// after the preceding kernel finished.
+// One kernel, grid (S, M), S = ceil(N / 8192) slices per row:
+//  1. CTA (s, m) reads slice s of row m, 32 logits per thread (thread t owns
+//     runs of 4 consecutive logits starting at 4t, 4t + 1024, ...), and each
+//     thread keeps the largest of its candidates.
+//  2. A lower bound for the slice's 32nd candidate: the 32nd largest of the 256
+//     per-thread maxima (warp sorts, then merges).  Those 32 maxima are distinct
+//     candidates at or above the bound, so the slice's top 32 are all at or
+//     above it; and only the 32 threads whose maximum reaches the bound can hold
+//     such candidates, so at most 32 * 32 = 1024 pass -- the candidate buffer
+//     never overflows, whatever the data.  The slice is read a second time
+//     (from L1) to collect them.
+//  3. The passing candidates are sorted in chunks of 32 by the warps (bitonic
+//     networks on shuffles), the chunks' top 32 merged, and the slice's top 32
+//     written to scratch.
+//  4. The last CTA of the row to finish (an acq_rel ticket) merges the S sorted
+//     lists (the top 32 of the union of two sorted lists is the elementwise
+//     maximum of one list and the other reversed, merged bitonically), and one
+//     warp forms the probabilities in double:
+//     p_j = exp((l_j - l_0)/T) / sum_i exp((l_i - l_0)/T) over the top_k, the
+//     shortest prefix whose cumulative probability reaches top_p kept (all if
+//     top_p >= 1), renormalized; fp32 probabilities and int32 indices out
+//     (-1 past top_k, probability 0 past the kept prefix).
+// The kernel uses programmatic dependent launch and reads the logits only after
+// the preceding kernel finished.  No thread waits on another CTA.
 #pragma once
 
 #include <cstdint>
@@ -30,12 +40,15 @@
 namespace q4 {
 namespace topk {
 
-constexpr int kWidth = 32;                 // candidates per slice and output entries per row
-constexpr int kMaxSlice = 16384;           // logits per slice (64 KB of keys in shared memory)
-constexpr int kMaxSlices = 64;             // slices per row (N <= kMaxSlice * kMaxSlices)
-constexpr int kSliceThreads = 512;
-constexpr int kMergeThreads = 256;
-constexpr int kSliceWarps = kSliceThreads / 32;
+constexpr int kWidth = 32;                    // candidates per slice and output entries per row
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPer = 32;                      // logits per thread
+constexpr int kRuns = kPer / 4;               // runs of 4 consecutive logits per thread
+constexpr int kSlice = kThreads * kPer;       // logits per CTA
+constexpr int kMaxSlices = 128;               // N <= kSlice * kMaxSlices
+constexpr int kCap = 32 * kPer;               // most candidates that can reach the bound
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ uint32_t monotone_key(float f) {
     const uint32_t u = __float_as_uint(f + 0.0f);  // -0 -> +0
@@ -47,20 +60,65 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float(u);
 }
 
-inline size_t slice_smem_bytes() {
-    return (size_t)kMaxSlice * 4 + (size_t)kSliceWarps * 256 * 4 + 256 * 4 + 2 * kSliceThreads * 4 + 64;
+__device__ __forceinline__ uint64_t candidate(uint32_t key, int64_t index) {
+    return ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)index);
 }
 
-// cand: [M][S][32] 64-bit candidates (0 = empty).
-__global__ void __launch_bounds__(kSliceThreads) topk_slice_kernel(const float* __restrict__ logits, int64_t N,
-                                                                   int64_t L, uint64_t* __restrict__ cand) {
-    extern __shared__ uint32_t sm[];
-    uint32_t* keys = sm;                                     // [kMaxSlice]
-    uint32_t* whist = keys + kMaxSlice;                      // [warps][256]
-    uint32_t* hist = whist + kSliceWarps * 256;              // [256]
-    uint32_t* cnt_gt = hist + 256;                           // [threads]
-    uint32_t* cnt_eq = cnt_gt + kSliceThreads;               // [threads]
-    __shared__ uint32_t sel_prefix, sel_need;
+__device__ __forceinline__ uint64_t umax(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t umin(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// One value per lane; returns the warp's values sorted descending by lane.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint64_t o = __shfl_xor_sync(kFull, v, stride);
+            const bool lower = (lane & stride) == 0;
+            const bool desc = (lane & size) == 0;   // the block's direction; size 32 is all descending
+            v = (lower == desc) ? umax(v, o) : umin(v, o);
+        }
+    }
+    return v;
+}
+
+// A bitonic sequence across the warp, sorted descending.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const uint64_t o = __shfl_xor_sync(kFull, v, stride);
+        v = (lane & stride) == 0 ? umax(v, o) : umin(v, o);
+    }
+    return v;
+}
+
+// Logits i .. i+3 of a slice (those past len are not read).
+__device__ __forceinline__ void load_run(const float* row, int i, int len, bool vec, float (&v)[4]) {
+    if (vec) {
+        if (i < len) {
+            const float4 q = *reinterpret_cast<const float4*>(row + i);
+            v[0] = q.x;
+            v[1] = q.y;
+            v[2] = q.z;
+            v[3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i + e < len) v[e] = row[i + e];
+    }
+}
+
+// cand: [M][S][32] scratch; tickets: [M] counters, zero between launches.
+// idx, probs: [M][32].
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restrict__ logits, int64_t N, int64_t L,
+                                                        int top_k, float temperature, float top_p,
+                                                        uint64_t* __restrict__ cand, int* __restrict__ tickets,
+                                                        int32_t* __restrict__ idx, float* __restrict__ probs) {
+    __shared__ uint64_t buf[kCap];
+    __shared__ uint64_t lists[kWarps][32];
+    __shared__ uint64_t bound;
+    __shared__ int count, is_last;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the logits come from the preceding kernel
     const int s = (int)blockIdx.x, m = (int)blockIdx.y;
@@ -69,141 +127,129 @@ __global__ void __launch_bounds__(kSliceThreads) topk_slice_kernel(const float* 
     const int64_t base = (int64_t)s * L;
     const int len = (int)((base + L <= N) ? L : (N - base));
     const float* row = logits + (int64_t)m * N + base;
-    for (int i = tid; i < len; i += kSliceThreads) keys[i] = monotone_key(row[i]);
-    const int k = len < kWidth ? len : kWidth;
+    if (tid == 0) count = 0;
 
-    // radix select of the k-th largest key, most significant digit first
-    uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
-    for (int d = 3; d >= 0; --d) {
-        uint32_t* wh = whist + warp * 256;
-        for (int b = lane; b < 256; b += 32) wh[b] = 0;
-        __syncthreads();                                     // keys staged, histograms cleared
-        const int sh = 8 * d;
-        for (int i = tid; i < len; i += kSliceThreads) {
-            const uint32_t key = keys[i];
-            if ((key & mask) == prefix) atomicAdd(&wh[(key >> sh) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 256) {
-            uint32_t h = 0;
-            for (int w = 0; w < kSliceWarps; ++w) h += whist[w * 256 + tid];
-            hist[tid] = h;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t cum = 0, nd = need;
-            int b = 255;
-            for (; b > 0; --b) {
-                if (cum + hist[b] >= nd) break;
-                cum += hist[b];
-            }
-            sel_prefix = prefix | ((uint32_t)b << sh);
-            sel_need = nd - cum;                             // how many keys equal to the prefix so far are needed
-        }
-        __syncthreads();
-        prefix = sel_prefix;
-        need = sel_need;
-        mask |= 255u << sh;
+    // 1. each thread's largest candidate (its bucket: 8 runs of 4 consecutive logits)
+    const bool vec = ((N | L) & 3) == 0;                       // rows and slices 16-byte aligned
+    uint64_t mx = 0;
+#pragma unroll
+    for (int c = 0; c < kRuns; ++c) {
+        const int i = 4 * (c * kThreads + tid);
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        load_run(row, i, len, vec, v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i + e < len) mx = umax(mx, candidate(monotone_key(v[e]), base + i + e));
     }
-    // prefix is now the k-th largest key; keys above it all enter, then the
-    // `need` lowest-index keys equal to it.  Each thread takes a contiguous chunk.
-    const int chunk = (len + kSliceThreads - 1) / kSliceThreads;
-    const int i0 = tid * chunk, i1 = (i0 + chunk < len) ? i0 + chunk : len;
-    uint32_t ngt = 0, neq = 0;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t key = keys[i];
-        ngt += key > prefix;
-        neq += key == prefix;
-    }
-    cnt_gt[tid] = ngt;
-    cnt_eq[tid] = neq;
-    __syncthreads();
-    if (tid == 0) {                                          // exclusive scans in thread order
-        uint32_t a = 0, b = 0;
-        for (int t = 0; t < kSliceThreads; ++t) {
-            const uint32_t x = cnt_gt[t], y = cnt_eq[t];
-            cnt_gt[t] = a;
-            cnt_eq[t] = b;
-            a += x;
-            b += y;
-        }
-    }
-    __syncthreads();
-    uint64_t* out = cand + ((int64_t)m * S + s) * kWidth;
-    const uint32_t n_gt = (uint32_t)k - need;                // keys strictly above the threshold
-    uint32_t pg = cnt_gt[tid], pe = cnt_eq[tid];
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t key = keys[i];
-        const uint64_t c = ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)(base + i));
-        if (key > prefix) {
-            out[pg++] = c;
-        } else if (key == prefix) {
-            if (pe < need) out[n_gt + pe] = c;
-            ++pe;
-        }
-    }
-    for (int j = k + tid; j < kWidth; j += kSliceThreads) out[j] = 0ull;
-}
 
-// idx, probs: [M][32].
-__global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const uint64_t* __restrict__ cand, int S, int top_k,
-                                                                   float temperature, float top_p,
-                                                                   int32_t* __restrict__ idx,
-                                                                   float* __restrict__ probs) {
-    __shared__ uint64_t c[kMaxSlices * kWidth];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");      // candidates come from the slice kernel
-    const int m = (int)blockIdx.x;
-    const int n = S * kWidth;
-    int P = 1;
-    while (P < n) P <<= 1;                                   // padded to a power of two with empty (0) entries
-    for (int i = threadIdx.x; i < P; i += kMergeThreads) c[i] = i < n ? cand[(int64_t)m * n + i] : 0ull;
+    // 2. the bound: 32nd largest of the per-thread maxima (0 if fewer than 32 threads hold logits)
+    mx = warp_sort_desc(mx, lane);
+    lists[warp][lane] = mx;
     __syncthreads();
-    // bitonic sort, descending
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < P; i += kMergeThreads) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;
-                    const uint64_t a = c[i], b = c[j];
-                    if (desc ? (a < b) : (a > b)) {
-                        c[i] = b;
-                        c[j] = a;
-                    }
-                }
-            }
-            __syncthreads();
-        }
+    if (warp == 0) {
+        uint64_t a = lists[0][lane];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) a = warp_merge_desc(umax(a, lists[w][31 - lane]), lane);
+        const uint64_t b = __shfl_sync(kFull, a, 31);
+        if (lane == 0) bound = b;
     }
-    if (threadIdx.x == 0) {
-        double e[kWidth];
-        const double l0 = (double)key_value((uint32_t)(c[0] >> 32));
-        const double t = (double)temperature;
-        double total = 0.0;
-        for (int j = 0; j < top_k; ++j) {
-            e[j] = exp(((double)key_value((uint32_t)(c[j] >> 32)) - l0) / t);
-            total += e[j];
-        }
-        for (int j = 0; j < top_k; ++j) e[j] = e[j] / total;
-        int keep = top_k;
-        if (top_p < 1.0f) {
-            double cum = 0.0;
-            for (int j = 0; j < top_k; ++j) {
-                cum += e[j];
-                if (cum >= (double)top_p) {
-                    keep = j + 1;
-                    break;
-                }
+    __syncthreads();
+    const uint64_t lb = bound;
+    // the slice again (the CTA's own recent reads: from L1), candidates at or above the bound
+#pragma unroll
+    for (int c = 0; c < kRuns; ++c) {
+        const int i = 4 * (c * kThreads + tid);
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        load_run(row, i, len, vec, v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (i + e < len) {
+                const uint64_t cv = candidate(monotone_key(v[e]), base + i + e);
+                if (cv >= lb) buf[atomicAdd(&count, 1)] = cv;
             }
         }
-        double kept = 0.0;
-        for (int j = 0; j < keep; ++j) kept += e[j];
-        for (int j = 0; j < kWidth; ++j) {
-            idx[m * kWidth + j] = j < top_k ? (int32_t)(~(uint32_t)(c[j] & 0xFFFFFFFFull)) : -1;
-            probs[m * kWidth + j] = j < keep ? (float)(e[j] / kept) : 0.0f;
+    }
+    __syncthreads();
+
+    // 3. the slice's top 32: warp w sorts chunks w, w + 8, ... of 32 candidates and
+    //    keeps the top 32 of them; the warps' lists are then merged by warp 0
+    const int n = count;
+    const int nch = (n + 31) / 32;
+    uint64_t a = 0;                                            // an empty list is all zeros
+    for (int ch = warp; ch < nch; ch += kWarps) {
+        const int i = ch * 32 + lane;
+        const uint64_t b = warp_sort_desc(i < n ? buf[i] : 0ull, lane);
+        a = warp_merge_desc(umax(a, __shfl_sync(kFull, b, 31 - lane)), lane);
+    }
+    if (nch > 1) {                                             // uniform: n is read by every thread
+        lists[warp][lane] = a;
+        __syncthreads();
+        if (warp == 0) {
+            const int nw = nch < kWarps ? nch : kWarps;
+            for (int w = 1; w < nw; ++w) a = warp_merge_desc(umax(a, lists[w][31 - lane]), lane);
         }
     }
+
+    // 4. publish the slice's top 32 (warp 0); the row's last CTA merges.  The warp
+    //    barrier orders the lanes' stores before lane 0's release of the ticket.
+    uint64_t* row_cand = cand + (int64_t)m * S * kWidth;
+    if (warp == 0) {
+        __stcg(row_cand + (int64_t)s * kWidth + lane, a);
+        __syncwarp();
+        if (lane == 0) {
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(tickets + m) : "memory");
+            const int lst = old == S - 1;
+            if (lst) asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(tickets + m) : "memory");
+            is_last = lst;
+        }
+    }
+    __syncthreads();                                           // lane 0's acquire, then the barrier, orders the
+    if (!is_last) return;                                      // other CTAs' lists before the reads below
+
+    // warp w merges lists w, w + 8, ..., loading four at a time
+    a = 0;
+    for (int l0 = warp; l0 < S; l0 += 4 * kWarps) {
+        uint64_t r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int l = l0 + u * kWarps;
+            r[u] = l < S ? __ldcg(row_cand + (int64_t)l * kWidth + (31 - lane)) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a = warp_merge_desc(umax(a, r[u]), lane);
+    }
+    lists[warp][lane] = a;
+    __syncthreads();
+    if (warp != 0) return;
+    a = lists[0][lane];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) a = warp_merge_desc(umax(a, lists[w][31 - lane]), lane);
+
+    // lane j holds the rank-j candidate.  Probabilities in double: exponentials
+    // lane-parallel, the sum as a butterfly and the cumulative sums as a scan (a
+    // fixed order; it differs from a left-to-right sum by double roundings only)
+    const double l0 = (double)key_value((uint32_t)(__shfl_sync(kFull, a, 0) >> 32));
+    const double lj = (double)key_value((uint32_t)(a >> 32));
+    const double e = lane < top_k ? exp((lj - l0) / (double)temperature) : 0.0;
+    double total = e;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
+    const double pj = e / total;
+    double cum = pj;                                           // inclusive scan over ranks
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(kFull, cum, o);
+        if (lane >= o) cum += t;
+    }
+    int keep = top_k;
+    if (top_p < 1.0f) {
+        const unsigned reach = __ballot_sync(kFull, lane < top_k && cum >= (double)top_p);
+        if (reach) keep = __ffs(reach);                        // the entry that reaches top_p is kept
+    }
+    const double kept = __shfl_sync(kFull, cum, keep - 1);
+    idx[m * kWidth + lane] = lane < top_k ? (int32_t)(~(uint32_t)(a & 0xFFFFFFFFull)) : -1;
+    probs[m * kWidth + lane] = lane < keep ? (float)(pj / kept) : 0.0f;
 }
 
 }  // namespace topk

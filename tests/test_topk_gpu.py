@@ -42,7 +42,8 @@ def _logits(M, N, seed, ties=True):
 def _check(y, k, temp, p):
     idx, pr = q4.topk_probs(y.cuda(), k, temp, p)
     q4.device_status()
-    ref_i, ref_p = T.topk_probs(y.numpy(), k, temp, p)
+    # the library takes temperature and top_p as fp32: the oracle gets the same values
+    ref_i, ref_p = T.topk_probs(y.numpy(), k, float(np.float32(temp)), float(np.float32(p)))
     assert np.array_equal(idx.cpu().numpy(), ref_i), "indices differ from the oracle"
     got = pr.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - ref_p) <= 2.0 * np.spacing(np.float32(np.maximum(ref_p, 1e-38))) + 1e-45)
@@ -54,9 +55,31 @@ def test_lm_head_rows_against_oracle(M, k, temp, p):
     _check(_logits(M, VOCAB, 100 + M + k), k, temp, p)
 
 
-@pytest.mark.parametrize("N", [32, 100, 16384, 16385, 40000])
+@pytest.mark.parametrize("N", [7, 32, 100, 8192, 8193, 16384, 16385, 40000])
 def test_small_and_ragged_rows(N):
     _check(_logits(4, N, N, ties=N > 20000), 32 if N >= 32 else N, 1.3, 0.9)
+
+
+@pytest.mark.parametrize("pattern", ["ascending", "descending", "crowded_threads", "plateau"])
+def test_adversarial_orders(pattern):
+    """Orders that defeat a bound taken from per-thread maxima as far as it can
+    be defeated: sorted rows, the largest logits crowded into few threads of a
+    slice (every candidate of 32 threads passes), and a plateau of equal values
+    just below a few larger ones."""
+    M, N = 3, 50000
+    g = torch.Generator().manual_seed(3)
+    y = torch.randn((M, N), generator=g).to(torch.float32)
+    if pattern == "ascending":
+        y = torch.sort(y, dim=1).values
+    elif pattern == "descending":
+        y = torch.sort(y, dim=1, descending=True).values
+    elif pattern == "crowded_threads":
+        pos = torch.arange(N)
+        y[:, (pos % 256) < 32] += 100.0          # thread-strided positions of the first 32 threads of each slice
+    else:
+        y[:, ::3] = 2.0
+        y[:, 1000:1005] = 3.0
+    _check(y, 32, 1.1, 0.97)
 
 
 def test_all_equal_logits():
