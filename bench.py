@@ -8,12 +8,17 @@ graph and replayed.  value = algorithmic HBM bytes of the step / device time,
 bytes per call = N*K*0.5625 + M*K*2 + M*N*4 (weights once, x once, y once).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload attn_sweep|lm_head|mlp_gdn|full_pass]
+                    [--workload attn_sweep|lm_head|mlp_gdn|full_pass|draft_edges]
 
 full_pass: one step = the whole 27B-shaped verify pass through q4_decode_step
 (64 layers x [in-proj, out-proj, gate/up, down] + the LM head twice, M = 16,
 glue between layers), captured once in a CUDA graph; value = 15,149,629,440
 weight bytes + activations and outputs per step / device time.
+
+draft_edges: one step = `reps` calls of q4_draft_select_edges (4 lanes x 7 draft
+positions, 16 x 16 edges each, rank 256, two 248,320 x 256 bf16 codebooks),
+each timed alone after an L2 flush; value = algorithmic bytes (the 32 gathered
+codebook rows, hidden, ids and scores of every row) / device time.
 
 Under torchrun each rank runs its own replica (the path needs no exchange);
 rank 0 prints one JSON line with the max-over-ranks time.
@@ -44,7 +49,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["attn_sweep", "lm_head", "mlp_gdn", "full_pass"], default="attn_sweep")
+    p.add_argument("--workload", choices=["attn_sweep", "lm_head", "mlp_gdn", "full_pass", "draft_edges"], default="attn_sweep")
     p.add_argument("--reps", type=int, default=20, help="calls per M per step")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -215,6 +220,9 @@ def run_reference(args, rank, world):
     """The oracle as the reference arm, on the host cores (rank 0 only)."""
     if rank != 0:
         return
+    if args.workload == "draft_edges":
+        run_reference_edges(args, world)
+        return
     spec, desc = workload_spec(args.workload)
     per_step = []
     walls = []
@@ -232,6 +240,34 @@ def run_reference(args, rank, world):
             "ms_per_step": round(1e3 * statistics.mean(walls[args.warmup:]), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": desc, "N": N, "K": K, "M": Ms},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": value,
+                             "unit": "GB/s"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_edges(args, world):
+    """The edge-score oracle as the reference arm (host cores, rank 0)."""
+    import numpy as np
+    import torch
+    import synth_inputs as si
+    V, R = si.VOCAB, si.EDGE_RANK
+    pb = si.make_codebook(V, R, 6001).view(torch.int16).numpy().view(np.uint16)
+    sb = si.make_codebook(V, R, 6002).view(torch.int16).numpy().view(np.uint16)
+    inputs = [si.make_edge_inputs(4, V, R, 7000 + k) for k in range(4)]
+    vals, walls, cb = [], [], None
+    for _ in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        cb = cpu_edges_sample(pb, sb, inputs, max(0.5, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup))))
+        walls.append(time.perf_counter() - t0)
+        vals.append(cb["value"])
+    value = statistics.mean(vals[args.warmup:])
+    line = {"impl": "reference", "metric": EDGE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.mean(walls[args.warmup:]), 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"draft_select_edges: 4 lanes x 7 positions, 16 x 16 edges, rank {R}, "
+                                   f"codebooks {V} x {R} bf16"},
             "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": value,
                              "unit": "GB/s"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -551,6 +587,151 @@ def run_full_pass(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+EDGE_METRIC = "draft_select_edges: algorithmic GB/s of the gathered codebook rows, hidden, ids and scores"
+
+
+def edge_call_bytes(rows, R):
+    return rows * (32 * R * 2 + R * 4 + 2 * 16 * 4 + 256 * 4)
+
+
+def cpu_edges_sample(P_bits, S_bits, inputs, seconds):
+    """The edge-score oracle timed on the host on successive calls of the workload
+    until about `seconds` have passed."""
+    import numpy as np
+    from oracle import edges as E
+    calls, byts = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        hidden, pred, cand = inputs[calls % len(inputs)]
+        E.edge_scores(P_bits, S_bits, hidden.numpy(), pred.numpy(), cand.numpy())
+        calls += 1
+        byts += edge_call_bytes(hidden.shape[0], hidden.shape[1])
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(byts / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} calls of the workload (4 lanes x 7 positions), fp64 oracle, one thread",
+            "ms_per_call": round(dt / calls * 1e3, 2)}
+
+
+def run_edges(args, rank, world, local_rank):
+    """The draft selector's edge scores: 4 lanes x 7 positions per call."""
+    import numpy as np
+    import torch
+    import bit_row_speculative_gb300 as q4
+    import synth_inputs as si
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    V, R, lanes = si.VOCAB, si.EDGE_RANK, 4
+    rows = lanes * si.EDGE_POSITIONS
+    P = si.make_codebook(V, R, 6001 + 7 * rank, device=dev)
+    S = si.make_codebook(V, R, 6002 + 7 * rank, device=dev)
+    host_inputs = [si.make_edge_inputs(lanes, V, R, 7000 + k) for k in range(16)]
+    dev_inputs = [tuple(t.to(dev) for t in inp) for inp in host_inputs]
+    score = torch.empty((rows, 16, 16), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)       # written between timed calls
+    call_b = edge_call_bytes(rows, R)
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(k):
+        h, pr, ca = dev_inputs[k % len(dev_inputs)]
+        q4.draft_select_edges(P, S, h, pr, ca, score=score, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup * args.reps):
+            call(k)
+    stream.synchronize()
+    q4.device_status(stream)
+    n = args.steps * args.reps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for k in range(n):
+            flush.fill_(k & 255)
+            evs[k][0].record(stream)
+            call(k)
+            evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    q4.device_status(stream)
+    if world > 1:
+        torch.distributed.barrier()
+    call_ms = [a.elapsed_time(b) for a, b in evs]
+    kernel_ms = max_over_ranks(sum(call_ms), world, dev)
+    value = job_throughput(call_b * args.reps, args.steps, kernel_ms, world)
+
+    # end to end through the public call: pinned host hidden and ids -> device,
+    # the call, scores -> pinned host, every call
+    hh = [tuple(t.pin_memory() for t in inp) for inp in host_inputs]
+    hs = torch.empty(score.shape, dtype=score.dtype).pin_memory()
+    dh, dp, dc = (torch.empty_like(t) for t in dev_inputs[0])
+    e_calls = 50
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for k in range(e_calls + 1):
+            if k == 1:
+                e0.record(stream)
+            h, pr, ca = hh[k % len(hh)]
+            dh.copy_(h, non_blocking=True)
+            dp.copy_(pr, non_blocking=True)
+            dc.copy_(ca, non_blocking=True)
+            q4.draft_select_edges(P, S, dh, dp, dc, score=score, stream=stream)
+            hs.copy_(score, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_calls, world, dev)
+    e2e = {"value": round(job_throughput(call_b, 1, e_ms, world), 2), "unit": "GB/s",
+           "h2d_bytes_per_step": (dh.numel() * 4 + dp.numel() * 4 + dc.numel() * 4) * args.reps,
+           "d2h_bytes_per_step": hs.numel() * 4 * args.reps, "us_per_call": round(e_ms * 1e3, 3)}
+
+    if rank != 0:
+        return
+    us = kernel_ms / n * 1e3
+    achieved = call_b / (us * 1e-6) / 1e9
+    line = {
+        "metric": EDGE_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(kernel_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 codebooks, fp32 hidden and accumulate",
+        "data": "synthetic (seeded; codebooks N(0,1)*0.05 bf16, hidden N(0,1), 16 distinct candidates per position, "
+                "predecessors = the previous position's candidates, the anchor at position 0)",
+        "config": {"workload": f"draft_select_edges: {lanes} lanes x {si.EDGE_POSITIONS} positions, 16 x 16 edges, "
+                               f"rank {R}, codebooks {V} x {R} bf16 (2 x {V * R * 2 / 1e6:.0f} MB)",
+                   "calls_per_step": args.reps,
+                   "l2": f"L2 flushed ({2 * l2 / 2**20:.0f} MiB written) before every timed call",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": {"mean": round(us, 3), "median": round(statistics.median(call_ms) * 1e3, 3),
+                        "min": round(min(call_ms) * 1e3, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 5), "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": call_b,
+                     "note": "one CTA per row gathers 32 rows of 512 B: latency-bound at this size"},
+        "gpu_launches": n,
+        "clocks": clocks, "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            pb = P.cpu().view(torch.int16).numpy().view(np.uint16)
+            sb = S.cpu().view(torch.int16).numpy().view(np.uint16)
+            line["cpu_baseline"] = cpu_edges_sample(pb, sb, host_inputs, min(args.cpu_seconds, 10.0))
+        except Exception as exc:                     # report, do not hide
+            line["cpu_baseline"] = {"error": repr(exc)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -567,6 +748,8 @@ def main():
     try:
         if args.workload == "full_pass":
             run_full_pass(args, rank, world, local_rank)
+        elif args.workload == "draft_edges":
+            run_edges(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

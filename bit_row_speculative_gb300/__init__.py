@@ -24,12 +24,13 @@ Q4_ERR_UNSUPPORTED_DEVICE = 4
 Q4_ERR_CUDA = 5
 Q4_ERR_TIMEOUT = 6
 Q4_ERR_OVERFLOW = 7
+Q4_ERR_INVALID_INDEX = 8
 MAX_ROWS = 16
 GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).
 SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_glue", "q4_decode_step_workspace_bytes",
-           "q4_decode_step", "q4_topk_probs", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
+           "q4_decode_step", "q4_topk_probs", "q4_draft_select_edges", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
 
 GLUE_NONE = 0
 GLUE_RMSNORM = 1
@@ -69,6 +70,9 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.q4_topk_probs.restype = c.c_int
     lib.q4_topk_probs.argtypes = [c.c_void_p, c.c_int, c.c_int64, c.c_int, c.c_float, c.c_float, c.c_void_p,
                                   c.c_void_p, c.c_void_p]
+    lib.q4_draft_select_edges.restype = c.c_int
+    lib.q4_draft_select_edges.argtypes = [c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_void_p, c.c_void_p,
+                                          c.c_void_p, c.c_int, c.c_void_p, c.c_void_p]
     lib.q4_check_wait_timeout.restype = c.c_int
     lib.q4_check_wait_timeout.argtypes = [c.c_longlong, c.c_void_p]
     lib.q4_device_status.restype = c.c_int
@@ -219,6 +223,20 @@ def topk_probs(logits, top_k: int, temperature: float, top_p: float, idx=None, p
     return idx, probs
 
 
+def draft_select_edges(pred_cb, succ_cb, hidden, pred_ids, cand_ids, score=None, stream=None):
+    """Edge scores fp32 [rows, 16, 16] of bf16 codebooks [V, R], fp32 hidden [rows, R]
+    and int32 ids [rows, 16] (all device tensors)."""
+    import torch
+    V, R = pred_cb.shape
+    rows = hidden.shape[0]
+    if score is None:
+        score = torch.empty((rows, 16, 16), dtype=torch.float32, device=hidden.device)
+    _check(lib().q4_draft_select_edges(pred_cb.data_ptr(), succ_cb.data_ptr(), V, R, hidden.data_ptr(),
+                                       pred_ids.data_ptr(), cand_ids.data_ptr(), rows, score.data_ptr(),
+                                       _stream_handle(stream)))
+    return score
+
+
 def check_wait_timeout(limit_cycles: int, stream=None) -> None:
     """Launch the timeout self-check: a bounded wait that runs out after
     `limit_cycles` and is then reported by device_status()."""
@@ -226,5 +244,6 @@ def check_wait_timeout(limit_cycles: int, stream=None) -> None:
 
 
 def device_status(stream=None) -> None:
-    """Synchronise and raise Q4Error(Q4_ERR_TIMEOUT) if a device-side wait gave up."""
+    """Synchronise and raise Q4Error (Q4_ERR_INVALID_INDEX for an out-of-range codebook id,
+    Q4_ERR_TIMEOUT for a device-side wait that gave up) if a kernel recorded one."""
     _check(lib().q4_device_status(_stream_handle(stream)))

@@ -20,6 +20,7 @@
 #include "q4_tm.cuh"
 #include "q4_glue.cuh"
 #include "q4_topk.cuh"
+#include "q4_edges.cuh"
 
 // Set by a kernel whose bounded device-side wait ran out (never by a trap).
 __device__ unsigned int q4_device_error_word = 0;
@@ -732,6 +733,33 @@ q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float 
     return Q4_OK;
 }
 
+q4_status q4_draft_select_edges(const void* pred_cb, const void* succ_cb, int64_t V, int R, const float* hidden,
+                                const int32_t* pred_ids, const int32_t* cand_ids, int rows, float* score,
+                                q4_stream_t stream) {
+    g_last_error.clear();
+    using namespace q4::edges;
+    if (!pred_cb || !succ_cb || !hidden || !pred_ids || !cand_ids || !score)
+        return fail(Q4_ERR_INVALID_ARG, "null pointer argument");
+    if (V < 1 || V > (int64_t)INT32_MAX) return fail(Q4_ERR_INVALID_ARG, "V = %lld is outside 1..2^31-1", (long long)V);
+    if (R < 8 || R > kMaxRank || R % 8 != 0)
+        return fail(Q4_ERR_UNSUPPORTED_SHAPE, "R = %d is not a multiple of 8 in 8..%d", R, kMaxRank);
+    if (rows < 1 || rows > kMaxEdgeRows)
+        return fail(Q4_ERR_INVALID_ARG, "rows = %d is outside 1..%d", rows, kMaxEdgeRows);
+    if (!aligned16(pred_cb) || !aligned16(succ_cb) || !aligned16(hidden) || !aligned16(pred_ids) ||
+        !aligned16(cand_ids) || !aligned16(score))
+        return fail(Q4_ERR_MISALIGNED, "codebooks, hidden, ids and score must be 16-byte aligned");
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    q4_status s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    const cudaError_t e =
+        launch_pdl(edges_kernel, dim3((unsigned)rows), dim3(kThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+                   static_cast<const uint16_t*>(pred_cb), static_cast<const uint16_t*>(succ_cb), V, R, hidden,
+                   pred_ids, cand_ids, score, info->error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the edge-score kernel");
+    return Q4_OK;
+}
+
 q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream) {
     g_last_error.clear();
     if (limit_cycles < 1 || limit_cycles > (1ll << 32))
@@ -761,6 +789,8 @@ q4_status q4_device_status(q4_stream_t stream) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(q4_device_error_word, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (word & q4::edges::kErrBadIndex)
+            return fail(Q4_ERR_INVALID_INDEX, "a codebook id was outside 0..V-1 (error word 0x%x)", word);
         return fail(Q4_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
     }
     return Q4_OK;
@@ -783,6 +813,7 @@ const char* q4_status_string(q4_status s) {
         case Q4_ERR_CUDA: return "Q4_ERR_CUDA";
         case Q4_ERR_TIMEOUT: return "Q4_ERR_TIMEOUT";
         case Q4_ERR_OVERFLOW: return "Q4_ERR_OVERFLOW";
+        case Q4_ERR_INVALID_INDEX: return "Q4_ERR_INVALID_INDEX";
     }
     return "Q4_ERR_UNKNOWN";
 }

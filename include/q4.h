@@ -54,7 +54,8 @@ typedef enum {
     Q4_ERR_UNSUPPORTED_DEVICE = 4, /* the current device is not compute 10.3       */
     Q4_ERR_CUDA = 5,               /* a CUDA runtime call failed                   */
     Q4_ERR_TIMEOUT = 6,            /* a device-side wait gave up (q4_device_status) */
-    Q4_ERR_OVERFLOW = 7            /* a byte count does not fit in 64 bits          */
+    Q4_ERR_OVERFLOW = 7,           /* a byte count does not fit in 64 bits          */
+    Q4_ERR_INVALID_INDEX = 8       /* a codebook id was out of range (q4_device_status) */
 } q4_status;
 
 #define Q4_MAX_ROWS 16
@@ -177,6 +178,30 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
 q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float temperature, float top_p,
                         int32_t* idx, float* probs, q4_stream_t stream);
 
+/* Edge scores of the draft selector ("Splash engine" analysis, section "The
+ * draft is a small model with an unusual selector": the top 16 candidates of
+ * each draft position are scored against 16 predecessors by a trilinear form
+ * over two bf16 codebooks of vocabulary x 256).  For row r (one draft position
+ * of one lane), predecessor i and candidate j:
+ *   score[r][i][j] = sum_{d<R} pred_cb[pred_ids[r][i]][d] * hidden[r][d]
+ *                                * succ_cb[cand_ids[r][j]][d]
+ *   pred_cb, succ_cb : device, bf16 [V, R] row-major (the predecessor and the
+ *                      successor codebook), read only at the ids' rows.
+ *   V : 1 .. 2^31-1.   R : a multiple of 8 in 8..256 (256 on the pages).
+ *   hidden   : device, fp32 [rows, R] (the position's rank-R projection).
+ *   pred_ids, cand_ids : device, int32 [rows, 16].
+ *   rows : 1 .. 2^20.
+ *   score    : device, fp32 [rows, 16, 16] (written; caller-owned).
+ * fp32 arithmetic: the context pred * hidden rounded once, then fused
+ * multiply-adds in a fixed order; |error| <= (R/4 + 3) * 2^-24 * the sum over d
+ * of |term|.  Each row's scores depend on that row's inputs only.  An id
+ * outside 0..V-1 is not read (its codebook row counts as zeros) and the next
+ * q4_device_status() returns Q4_ERR_INVALID_INDEX.  All pointers 16-byte
+ * aligned.  Asynchronous on `stream`; no scratch. */
+q4_status q4_draft_select_edges(const void* pred_cb, const void* succ_cb, int64_t V, int R, const float* hidden,
+                                const int32_t* pred_ids, const int32_t* cand_ids, int rows, float* score,
+                                q4_stream_t stream);
+
 /* Self-check of the timeout reporting path.  Launches one thread on `stream`
  * that waits, with the same bounded wait every kernel of this library uses, on
  * a barrier that nothing signals; after `limit_cycles` SM clock cycles
@@ -187,8 +212,10 @@ q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float 
 q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream);
 
 /* Synchronizes `stream` and reports whether any kernel of this library on the
- * current device gave up a bounded device-side wait since the last query
- * (Q4_ERR_TIMEOUT), then clears that record.  Q4_OK otherwise. */
+ * current device recorded a device-side failure since the last query -- an
+ * out-of-range codebook id (Q4_ERR_INVALID_INDEX, reported first) or a bounded
+ * wait that gave up (Q4_ERR_TIMEOUT) -- then clears that record.  Q4_OK
+ * otherwise. */
 q4_status q4_device_status(q4_stream_t stream);
 
 /* Thread-local description of the last failure on this thread ("" if none). */

@@ -111,3 +111,37 @@ def full_pass_spec():
         spec += [(n_in, HIDDEN, 1), (HIDDEN, ATTN_OUT_IN, 1), (2 * INTERMEDIATE, HIDDEN, 2), (HIDDEN, INTERMEDIATE, 1)]
     spec += [(VOCAB, HIDDEN, 1), (VOCAB, HIDDEN, 0)]
     return spec
+
+
+# ------------------------------------------------------------ draft selector
+# Edge-score inputs: two bf16 codebooks [VOCAB, 256], each entry N(0,1) * 0.05
+# rounded to nearest even; per (lane, position) row a hidden projection of 256
+# N(0,1) fp32 values; the 16 candidates of a position are 16 distinct token ids
+# drawn uniformly; the predecessors of position p > 0 are the candidates of
+# position p - 1, and those of position 0 are the lane's anchor token, repeated.
+EDGE_RANK = 256
+EDGE_POSITIONS = 7
+EDGE_PAIRS = 16
+
+
+def make_codebook(V: int, R: int, seed: int, device="cpu") -> torch.Tensor:
+    g = _gen(seed, device)
+    return (torch.randn((V, R), generator=g, device=device, dtype=torch.float32) * 0.05).to(torch.bfloat16)
+
+
+def make_edge_inputs(lanes: int, V: int, R: int, seed: int, positions: int = EDGE_POSITIONS):
+    """(hidden fp32 [rows, R], pred_ids int32 [rows, 16], cand_ids int32 [rows, 16]) on the CPU,
+    rows = lanes * positions, row = lane * positions + position."""
+    g = _gen(seed, "cpu")
+    rows = lanes * positions
+    hidden = torch.randn((rows, R), generator=g, dtype=torch.float32)
+    cand = torch.empty((rows, EDGE_PAIRS), dtype=torch.int32)
+    pred = torch.empty((rows, EDGE_PAIRS), dtype=torch.int32)
+    for lane in range(lanes):
+        anchor = int(torch.randint(0, V, (1,), generator=g))
+        for p in range(positions):
+            r = lane * positions + p
+            cand[r] = torch.randperm(V, generator=g)[:EDGE_PAIRS].to(torch.int32) if V >= 4 * EDGE_PAIRS else \
+                torch.randint(0, V, (EDGE_PAIRS,), generator=g, dtype=torch.int32)
+            pred[r] = cand[r - 1] if p > 0 else torch.full((EDGE_PAIRS,), anchor, dtype=torch.int32)
+    return hidden, pred, cand

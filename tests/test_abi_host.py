@@ -148,3 +148,31 @@ def test_topk_rejects_bad_arguments(M, N, k, T, p, align, status):
     lib = q4.lib()
     rc = lib.q4_topk_probs(16 + align, M, N, k, T, p, 16, 16, None)
     assert rc == status, (rc, lib.q4_last_error())
+
+
+@pytest.mark.parametrize("V,R,rows,align,status", [
+    (0, 256, 7, 0, q4.Q4_ERR_INVALID_ARG),
+    (1 << 31, 256, 7, 0, q4.Q4_ERR_INVALID_ARG),
+    (100, 0, 7, 0, q4.Q4_ERR_UNSUPPORTED_SHAPE),
+    (100, 12, 7, 0, q4.Q4_ERR_UNSUPPORTED_SHAPE),
+    (100, 264, 7, 0, q4.Q4_ERR_UNSUPPORTED_SHAPE),
+    (100, 256, 0, 0, q4.Q4_ERR_INVALID_ARG),
+    (100, 256, (1 << 20) + 1, 0, q4.Q4_ERR_INVALID_ARG),
+    (100, 256, 7, 8, q4.Q4_ERR_MISALIGNED),
+])
+def test_edges_rejects_bad_arguments(V, R, rows, align, status):
+    lib = q4.lib()
+    rc = lib.q4_draft_select_edges(16 + align, 16, V, R, 16, 16, 16, rows, 16, None)
+    assert rc == status, (rc, lib.q4_last_error())
+
+
+def test_edges_rejects_null_pointers():
+    lib = q4.lib()
+    assert lib.q4_draft_select_edges(16, None, 100, 256, 16, 16, 16, 7, 16, None) == q4.Q4_ERR_INVALID_ARG
+
+
+def test_status_names_cover_every_code():
+    lib = q4.lib()
+    for code in range(0, 9):
+        assert lib.q4_status_string(code).decode().startswith("Q4_")
+        assert lib.q4_status_string(code).decode() != "Q4_ERR_UNKNOWN"
