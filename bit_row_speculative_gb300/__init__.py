@@ -25,7 +25,7 @@ Q4_ERR_CUDA = 5
 Q4_ERR_TIMEOUT = 6
 Q4_ERR_OVERFLOW = 7
 Q4_ERR_INVALID_INDEX = 8
-MAX_ROWS = 16
+MAX_ROWS = 32
 GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).

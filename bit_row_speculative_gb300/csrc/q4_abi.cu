@@ -104,7 +104,7 @@ cudaError_t prepare_tc() {
 template <int MT>
 cudaError_t prepare_tm() {
     return cudaFuncSetAttribute(q4::tm::q4_tm_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                q4::tm::smem_bytes());
+                                q4::tm::smem_bytes<MT>());
 }
 
 template <int MT>
@@ -138,6 +138,7 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_generic<4>();
             if (a == cudaSuccess) a = prepare_generic<8>();
             if (a == cudaSuccess) a = prepare_generic<16>();
+            if (a == cudaSuccess) a = prepare_generic<32>();
             if (a == cudaSuccess) a = prepare_tc<1>();
             if (a == cudaSuccess) a = prepare_tc<2>();
             if (a == cudaSuccess) a = prepare_tc<4>();
@@ -150,6 +151,8 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_tm<4>();
             if (a == cudaSuccess) a = prepare_tm<8>();
             if (a == cudaSuccess) a = prepare_tm<16>();
+            if (a == cudaSuccess) a = prepare_tm<24>();
+            if (a == cudaSuccess) a = prepare_tm<32>();
             if (a != cudaSuccess) return cuda_fail(a, "cudaFuncSetAttribute");
             if (!g_encode) {
                 void* fn = nullptr;
@@ -168,7 +171,8 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
                                   sizeof(int);
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
-            if (a == cudaSuccess) a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * q4::prep::kRecordBytes);
+            if (a == cudaSuccess)
+                a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * std::max(q4::prep::kRecordBytes, q4::tm::rec_bytes(32)));
             if (a == cudaSuccess)
                 a = cudaMalloc(&d.topk_cand, (size_t)Q4_MAX_ROWS * q4::topk::kMaxSlices * q4::topk::kWidth * sizeof(uint64_t));
             if (a == cudaSuccess) a = cudaMalloc(&d.topk_tickets, (size_t)Q4_MAX_ROWS * sizeof(int));
@@ -189,7 +193,9 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int rows_template(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+int rows_template(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32; }
+// the tensor-memory kernel also has a 24-row instance (same 32-row layout, fewer live accumulators)
+int tm_rows_template(int M) { return M <= 16 ? rows_template(M) : M <= 24 ? 24 : 32; }
 
 q4_status launch_generic(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                          cudaStream_t stream) {
@@ -206,7 +212,8 @@ q4_status launch_generic(const void* x, const void* W, int M, int64_t N, int64_t
         case 2: matmul_kernel<2><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
         case 4: matmul_kernel<4><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
         case 8: matmul_kernel<8><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
-        default: matmul_kernel<16><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+        case 16: matmul_kernel<16><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
+        default: matmul_kernel<32><<<grid, block, smem, stream>>>(xp, wp, M, N, K, y); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launching the generic Q4 kernel");
@@ -310,17 +317,21 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
 #ifdef Q4_TRACE
     p.trace = g_trace;
 #endif
-    cudaError_t e = launch_pdl(xrec_kernel, dim3((unsigned)p.G), dim3(kRecThreads), 0, stream,
-                               static_cast<const uint16_t*>(x), M, K, d.xt);
+    const int MT = tm_rows_template(M);
+    cudaError_t e = MT <= 16 ? launch_pdl(xrec_kernel<16>, dim3((unsigned)p.G), dim3(8 * 16), 0, stream,
+                                          static_cast<const uint16_t*>(x), M, K, d.xt)
+                             : launch_pdl(xrec_kernel<32>, dim3((unsigned)p.G), dim3(8 * 32), 0, stream,
+                                          static_cast<const uint16_t*>(x), M, K, d.xt);
     if (e != cudaSuccess) return cuda_fail(e, "launching the x record kernel");
     const dim3 grid((unsigned)p.C), block(kThreads);
-    const size_t smem = (size_t)smem_bytes();
-    switch (rows_template(M)) {
-        case 1: e = launch_pdl(q4_tm_kernel<1>, grid, block, smem, stream, map_nib, p); break;
-        case 2: e = launch_pdl(q4_tm_kernel<2>, grid, block, smem, stream, map_nib, p); break;
-        case 4: e = launch_pdl(q4_tm_kernel<4>, grid, block, smem, stream, map_nib, p); break;
-        case 8: e = launch_pdl(q4_tm_kernel<8>, grid, block, smem, stream, map_nib, p); break;
-        default: e = launch_pdl(q4_tm_kernel<16>, grid, block, smem, stream, map_nib, p); break;
+    switch (MT) {
+        case 1: e = launch_pdl(q4_tm_kernel<1>, grid, block, (size_t)smem_bytes<1>(), stream, map_nib, p); break;
+        case 2: e = launch_pdl(q4_tm_kernel<2>, grid, block, (size_t)smem_bytes<2>(), stream, map_nib, p); break;
+        case 4: e = launch_pdl(q4_tm_kernel<4>, grid, block, (size_t)smem_bytes<4>(), stream, map_nib, p); break;
+        case 8: e = launch_pdl(q4_tm_kernel<8>, grid, block, (size_t)smem_bytes<8>(), stream, map_nib, p); break;
+        case 16: e = launch_pdl(q4_tm_kernel<16>, grid, block, (size_t)smem_bytes<16>(), stream, map_nib, p); break;
+        case 24: e = launch_pdl(q4_tm_kernel<24>, grid, block, (size_t)smem_bytes<24>(), stream, map_nib, p); break;
+        default: e = launch_pdl(q4_tm_kernel<32>, grid, block, (size_t)smem_bytes<32>(), stream, map_nib, p); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the tensor-memory Q4 kernel");
     return Q4_OK;
@@ -379,8 +390,8 @@ q4_status dispatch_matmul(const DeviceInfo& d, const void* x, const void* W, int
             const char* v = std::getenv("Q4_ALT_KERNEL");
             return v ? std::atoi(v) : 0;
         }();
-        if (alt_kernel == 1) return launch_tc(d, x, W, M, N, K, y, stream);
-        if (alt_kernel == 2) return launch_rk(d, x, W, M, N, K, y, stream);
+        if (alt_kernel == 1 && M <= 16) return launch_tc(d, x, W, M, N, K, y, stream);
+        if (alt_kernel == 2 && M <= 16) return launch_rk(d, x, W, M, N, K, y, stream);
         return launch_tm(d, x, W, M, N, K, y, stream);
     }
     return launch_generic(x, W, M, N, K, y, stream);
@@ -474,6 +485,7 @@ void decode_workspace_layout(const q4_layer* layers, int n_layers, int M, size_t
 namespace {
 
 constexpr int kNoAllocMaxSms = 160;
+constexpr int kNoAllocMaxRows = 16;   // its two-launch kernel holds 16-row x records
 constexpr int64_t kNoAllocMaxK = 20480;
 constexpr size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 constexpr size_t kNoAllocPartialBytes =
@@ -533,6 +545,7 @@ q4_status noalloc_setup(const NoAllocDevice** out) {
             if (a == cudaSuccess) a = prepare_generic<4>();
             if (a == cudaSuccess) a = prepare_generic<8>();
             if (a == cudaSuccess) a = prepare_generic<16>();
+            if (a == cudaSuccess) a = prepare_generic<32>();
             if (a == cudaSuccess) a = prepare_tc<1>();
             if (a == cudaSuccess) a = prepare_tc<2>();
             if (a == cudaSuccess) a = prepare_tc<4>();
@@ -590,7 +603,8 @@ q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int6
                             q4_stream_t stream) {
     g_last_error.clear();
     if (!x || !W || !y) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (x=%p W=%p y=%p)", x, W, (void*)y);
-    if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
+    if (M < 1 || M > kNoAllocMaxRows)
+        return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d (q4_matmul_noalloc)", M, kNoAllocMaxRows);
     if (N < 1) return fail(Q4_ERR_INVALID_ARG, "N = %lld must be >= 1", (long long)N);
     if (K < 64 || (K % 64) != 0)
         return fail(Q4_ERR_UNSUPPORTED_SHAPE, "K = %lld must be a positive multiple of 64", (long long)K);

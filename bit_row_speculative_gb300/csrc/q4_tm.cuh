@@ -74,8 +74,6 @@ namespace tm {
 
 constexpr int kRowsTile = 128;              // rows per tile (tensor-memory lanes)
 constexpr int kTeams = 3;                   // consumer teams (one warpgroup each)
-constexpr int kStages = 12;                 // a multiple of kTeams
-static_assert(kStages % kTeams == 0, "each ring slot must belong to one team");
 constexpr int kIssuersPerTeam = 1;          // MMA issuing threads per team (they split the two groups)
 constexpr int kIssuers = kIssuersPerTeam * kTeams;
 constexpr int kConsumerWarp0 = 4;           // warps 4.. (warp % 4 = tensor-memory lane quarter)
@@ -83,22 +81,35 @@ constexpr int kThreads = (kConsumerWarp0 + 4 * kTeams) * 32;   // 512
 constexpr int kConsumerThreads = kTeams * 128;
 static_assert(kIssuers + 1 <= kConsumerWarp0, "control warps");
 
-constexpr int kRec = 2112;                            // x record of one group
-constexpr int kRecHalf = 1088;                        // X and rows 0-7
-constexpr int kRecB = 64;                             // offset of the core matrices in a record
+// Row width W: the x records and the MMAs cover W = 16 rows for M <= 16 and
+// W = 32 rows for 16 < M <= 32.  Everything of the layout below depends on W.
+template <int MT>
+__host__ __device__ constexpr int width() { return MT > 16 ? 32 : 16; }
+__host__ __device__ constexpr int rec_bytes(int W) { return 4 * W + (W / 8) * 1024; }   // X[W] fp32, then W/8 blocks of 8 rows
+__host__ __device__ constexpr int rec_b(int W) { return 4 * W; }                        // offset of the core matrices
+constexpr int kRecHalf = 1088;                        // W = 16: X and rows 0-7
 constexpr int kNibStage = kRowsTile * 64;             // 8 KB: 128 rows x 64 B (two groups)
-constexpr int kStageBytes = ((kNibStage + 2 * kRec + 1023) / 1024) * 1024;
-constexpr int kRedBytes = 2 * kTeams * 16 * kRowsTile * 4;   // team sums of a segment, two buffers
+__host__ __device__ constexpr int stage_bytes(int W) { return ((kNibStage + 2 * rec_bytes(W) + 1023) / 1024) * 1024; }
+__host__ __device__ constexpr int stages(int W) { return W == 16 ? 12 : 9; }            // a multiple of kTeams
+// team sums of a segment: two buffers used alternately at W = 16, one at W = 32
+__host__ __device__ constexpr int red_buffers(int W) { return W == 16 ? 2 : 1; }
+__host__ __device__ constexpr int red_bytes(int W) { return red_buffers(W) * kTeams * W * kRowsTile * 4; }
 constexpr int kBarrierBytes = 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + kRedBytes + kBarrierBytes + 1024 /* alignment slack */;
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+__host__ __device__ constexpr int smem_bytes_w(int W) {
+    return stages(W) * stage_bytes(W) + red_bytes(W) + kBarrierBytes + 1024 /* alignment slack */;
+}
+static_assert(stages(16) % kTeams == 0 && stages(32) % kTeams == 0, "each ring slot must belong to one team");
+static_assert(smem_bytes_w(16) <= 232448 && smem_bytes_w(32) <= 232448, "shared memory per CTA");
 
-// tensor-memory columns per team: A0, A1 (two groups x 32 each), P (two groups x 16)
+// tensor-memory columns per team: the dequantized A of a stage (two groups x
+// 32), twice at W = 16 (double-buffered), once at W = 32; then P (two groups x W)
 constexpr uint32_t kColsA = 64;
-constexpr uint32_t kColP = 2 * kColsA;
-constexpr uint32_t kColsTeam = kColP + 32;
+__host__ __device__ constexpr uint32_t a_buffers(int W) { return W == 16 ? 2 : 1; }
+__host__ __device__ constexpr uint32_t col_p(int W) { return a_buffers(W) * kColsA; }
+__host__ __device__ constexpr uint32_t cols_team(int W) { return col_p(W) + 2 * W; }
 constexpr uint32_t kTmemCols = 512;
-static_assert(kTeams * kColsTeam <= kTmemCols, "tensor memory over-subscribed");
+static_assert(kTeams * cols_team(16) <= kTmemCols && kTeams * cols_team(32) <= kTmemCols,
+              "tensor memory over-subscribed");
 
 constexpr long long kWaitLimit = 2000000000LL;     // cycles (about one second)
 constexpr float kFoldScale = 8589934592.0f;        // 2^33: undoes 2^-133 (weights) * 2^100 (x)
@@ -108,9 +119,9 @@ constexpr uint32_t kXScaleOdd = 0x6F806F80u;       // bf16 pair (2^96, 2^96)
 struct Params {
     const uint8_t* W;           // packed weights
     float* y;                   // [M, N]
-    float* partials;            // scratch: [C][2][16][128]
+    float* partials;            // scratch: [C][2][W][128]
     int* sems;                  // scratch: [C], zero between launches
-    const uint8_t* xt;          // x records [G][2112] (written by xrec_kernel)
+    const uint8_t* xt;          // x records [G][rec_bytes(W)] (written by xrec_kernel)
     unsigned int* error_word;   // set on a timed-out wait
     int64_t N;
     int64_t K;
@@ -219,12 +230,11 @@ __device__ __forceinline__ bool wait_or_abort(const Params& p, uint64_t* bar, ui
 }
 
 // ------------------------------------------------------------------ x records
-// One CTA per group of 64 inputs, 128 threads: thread t takes row m = t / 8
+// One CTA per group of 64 inputs, 8 * W threads: thread t takes row m = t / 8
 // and 8-block kc = t % 8 of the group.
-constexpr int kRecThreads = 128;
-
-__global__ void __launch_bounds__(kRecThreads) xrec_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
-                                                           uint8_t* __restrict__ xt) {
+template <int W>
+__global__ void __launch_bounds__(8 * W) xrec_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+                                                     uint8_t* __restrict__ xt) {
     pdl_launch_dependents();
     // x may come from the preceding kernel, and the preceding matmul may still
     // read the records of its own call: wait for it first
@@ -239,8 +249,8 @@ __global__ void __launch_bounds__(kRecThreads) xrec_kernel(const uint16_t* __res
     o.y = bf16x2_mul(prmt(v.x, v.z, 0x7632u), kXScaleOdd);     // (k1, k5)
     o.z = bf16x2_mul(prmt(v.y, v.w, 0x5410u), kXScaleEven);    // (k2, k6)
     o.w = bf16x2_mul(prmt(v.y, v.w, 0x7632u), kXScaleOdd);     // (k3, k7)
-    uint8_t* rec = xt + (int64_t)g * kRec;
-    *reinterpret_cast<uint4*>(rec + kRecB + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
+    uint8_t* rec = xt + (int64_t)g * rec_bytes(W);
+    *reinterpret_cast<uint4*>(rec + rec_b(W) + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
     // X: the 8 inputs in increasing k, then the 8 block sums of the row (in 8
     // consecutive lanes) by a fixed xor tree
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -325,10 +335,11 @@ __device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, 
 template <int MT>
 __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t, bool whole, int slot, int team,
                             int row, int c_id, int* bcast, bool live) {
-    // red: this segment's buffer (the caller alternates the two by segment)
+    // red: this segment's buffer (at W = 16 the caller alternates two by segment)
+    constexpr int W = width<MT>();
     constexpr int kJ = (MT + kTeams - 1) / kTeams;
 #pragma unroll
-    for (int m = 0; m < MT; ++m) red[(team * 16 + m) * kRowsTile + row] = acc[m];
+    for (int m = 0; m < MT; ++m) red[(team * W + m) * kRowsTile + row] = acc[m];
     named_barrier(1, kConsumerThreads);
     const int64_t n = (int64_t)t * kRowsTile + row;
     float v[kJ];
@@ -338,9 +349,11 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
         v[j] = 0.0f;
         if (m < MT) {
 #pragma unroll
-            for (int tm_ = 0; tm_ < kTeams; ++tm_) v[j] = __fadd_rn(v[j], red[(tm_ * 16 + m) * kRowsTile + row]);
+            for (int tm_ = 0; tm_ < kTeams; ++tm_) v[j] = __fadd_rn(v[j], red[(tm_ * W + m) * kRowsTile + row]);
         }
     }
+    // one buffer: every thread has read it before any thread writes it for the next segment
+    if (red_buffers(W) == 1) named_barrier(1, kConsumerThreads);
     if (whole) {
         if (live && n < p.N) {
 #pragma unroll
@@ -350,7 +363,7 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
             }
         }
     } else {
-        float* dst = p.partials + (((int64_t)c_id * 2 + slot) * 16) * kRowsTile + row;
+        float* dst = p.partials + (((int64_t)c_id * 2 + slot) * W) * kRowsTile + row;
         if (live) {
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
@@ -386,7 +399,7 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
             for (int c = c_first; c <= c_last; ++c) {
                 const int cs = range_start(p.U, p.C, c);
                 const int cslot = (cs / p.GP == t) ? 0 : 1;   // the tile is c's first segment, or its last
-                const float* src = p.partials + (((int64_t)c * 2 + cslot) * 16) * kRowsTile + row;
+                const float* src = p.partials + (((int64_t)c * 2 + cslot) * W) * kRowsTile + row;
 #pragma unroll
                 for (int j = 0; j < kJ; ++j) {
                     const int m = team + kTeams * j;
@@ -402,10 +415,11 @@ __device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t
             }
         }
     }
-    // red alternates between two buffers by segment, so a buffer is rewritten
-    // only after every thread has passed the first barrier of the segment
-    // between (and with it finished reading here); bcast is written only on
-    // the partial path, between two barriers
+    // At W = 16 red alternates between two buffers by segment, so a buffer is
+    // rewritten only after every thread has passed the first barrier of the
+    // segment between (and with it finished reading here); at W = 32 the
+    // barrier after the reads above does that.  bcast is written only on the
+    // partial path, between two barriers
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 }
@@ -414,6 +428,14 @@ template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
 q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     using namespace q4::sm100;
+    constexpr int W = width<MT>();
+    constexpr int kStages = stages(W);
+    constexpr int kStageBytes = stage_bytes(W);
+    constexpr int kRec = rec_bytes(W);
+    constexpr int kRecB = rec_b(W);
+    constexpr int kRedBytes = red_bytes(W);
+    constexpr uint32_t kColP = col_p(W);
+    constexpr uint32_t kColsTeam = cols_team(W);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes);
@@ -534,7 +556,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)(j & 1), 2u, abort_flag))) break;
             tc_fence_after();
             const uint64_t bd = bdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-            const uint32_t aS = tbase + (uint32_t)(j & 1) * kColsA;
+            const uint32_t aS = tbase + (a_buffers(W) == 2 ? (uint32_t)(j & 1) * kColsA : 0u);
             const uint32_t dS = tbase + kColP;
             if (lane == 0) {
                 if (team == 0 && gsel == 0) Q4_TMTR(p, 2000 + 2 * si);
@@ -542,9 +564,14 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                 for (int g = 0; g < 2; ++g) {
                     if (g % kIssuersPerTeam != gsel) continue;
                     const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
+                    // P of group g: W columns, rows 0-15 then (W = 32) rows 16-31 from the
+                    // record's second 2048 bytes -- the same N = 16 instruction for every row
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ts(dS + 16u * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
+                    for (int h = 0; h < W / 16; ++h)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_ts(dS + (uint32_t)W * g + 16u * h, aS + 32u * g + 8u * kk,
+                                      bg + (uint64_t)((2048 * h) >> 4) + 16u * kk, idesc, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&done[team]);
                 if (team == 0 && gsel == 0) Q4_TMTR(p, 2001 + 2 * si);
@@ -621,7 +648,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                 const int tt = t0 + cur_seg;
                 const bool whole = u0 <= tt * p.GP && (tt + 1) * p.GP <= u1;
                 if (team == 0 && row == 0 && cur_seg < 2) Q4_TMGT(p, 2403 + 8 * c_id + 2 * cur_seg);
-                end_segment<MT>(p, acc, red + (cur_seg & 1) * (kTeams * 16 * kRowsTile), tt, whole,
+                end_segment<MT>(p, acc, red + (red_buffers(W) == 2 ? (cur_seg & 1) : 0) * (kTeams * W * kRowsTile), tt, whole,
                                 cur_seg == 0 ? 0 : 1, team, row, c_id, bcast, !*abort_flag);
                 if (team == 0 && row == 0 && cur_seg < 2) {
                     Q4_TMGT(p, 2404 + 8 * c_id + 2 * cur_seg);
@@ -654,6 +681,15 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                     tmem_wait_ld();
                     fold_group<MT>(acc, P0, xs0, ps0, pr0);
                     fold_group<MT>(acc, P1, xs1, ps1, pr1);
+                } else if (W == 32) {
+                    // 32 columns per group, one group at a time (registers)
+                    uint32_t P[32];
+                    tmem_ld_32x32b_x32(dP, P);
+                    tmem_wait_ld();
+                    fold_group<MT>(acc, P, xs0, ps0, pr0);
+                    tmem_ld_32x32b_x32(dP + 32u, P);
+                    tmem_wait_ld();
+                    fold_group<MT>(acc, P, xs1, ps1, pr1);
                 } else {
                     uint32_t P0[16], P1[16];
                     tmem_ld_32x32b_x16(dP, P0);
@@ -679,11 +715,13 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 8u,
                                                                  abort_flag));
             Q4_TMTR(p, tr + 8 * j + 1);
-            // dequantize into this stage's A buffer (the other one may still feed the previous MMAs)
+            // one A buffer (W = 32): the previous stage's MMAs must have read it, so fold first
+            if (a_buffers(W) == 1 && pend >= 0) fold_pending();
+            // dequantize into this stage's A buffer (at W = 16 the other one may still feed the previous MMAs)
             if (live) {
                 const uint8_t* nb = smem + slot * kStageBytes + row * 64;
                 const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
-                const uint32_t aA = tbase + (uint32_t)(j & 1) * kColsA;
+                const uint32_t aA = tbase + (a_buffers(W) == 2 ? (uint32_t)(j & 1) * kColsA : 0u);
                 uint32_t av0[32], av1[32];
                 {
                     const uint4 na = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
@@ -701,7 +739,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             }
             Q4_TMTR(p, tr + 8 * j + 2);
             // fold the previous stage (its MMAs ran meanwhile); then P is free again
-            if (pend >= 0) fold_pending();
+            if (a_buffers(W) == 2 && pend >= 0) fold_pending();
             Q4_TMTR(p, tr + 8 * j + 3);
             tc_fence_before();
             __syncwarp();
@@ -745,8 +783,9 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     }
 }
 
-inline int smem_bytes() { return kSmemBytes; }
-inline size_t partial_floats(int C) { return (size_t)C * 2 * 16 * kRowsTile; }
+template <int MT>
+inline int smem_bytes() { return smem_bytes_w(width<MT>()); }
+inline size_t partial_floats(int C) { return (size_t)C * 2 * 32 * kRowsTile; }   // sized for W = 32
 inline size_t sem_ints(int C) { return (size_t)C; }
 
 }  // namespace tm

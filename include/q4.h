@@ -1,7 +1,7 @@
 /*
  * q4.h -- C ABI of the GB300 Q4 verify-matmul library (libq4.so).
  *
- * The operation.  A speculative-decoding verify pass multiplies M = 1..16 draft
+ * The operation.  A speculative-decoding verify pass multiplies M = 1..32 draft
  * or tree rows against every quantized weight of a layer, reading the weights
  * from HBM once ("Faster, with the same words" (goinfer.dev), section "The
  * problem": a step that checks eight tokens costs much less than eight steps,
@@ -48,7 +48,7 @@ typedef struct CUstream_st* q4_stream_t;
 
 typedef enum {
     Q4_OK = 0,
-    Q4_ERR_INVALID_ARG = 1,        /* null pointer, M out of 1..16, N < 1, ...     */
+    Q4_ERR_INVALID_ARG = 1,        /* null pointer, M out of 1..32, N < 1, ...     */
     Q4_ERR_UNSUPPORTED_SHAPE = 2,  /* K not a positive multiple of 64              */
     Q4_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned             */
     Q4_ERR_UNSUPPORTED_DEVICE = 4, /* the current device is not compute 10.3       */
@@ -58,7 +58,7 @@ typedef enum {
     Q4_ERR_INVALID_INDEX = 8       /* a codebook id was out of range (q4_device_status) */
 } q4_status;
 
-#define Q4_MAX_ROWS 16
+#define Q4_MAX_ROWS 32
 
 /* Bytes of a packed N x K matrix: the page's q4PackedBytes -- an
  * overflow-checked (N*K/16)*9 ("Splash engine", section "The engine hard-codes
@@ -69,8 +69,12 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
 /* y[M,N] = x[M,K] * W[N,K]^T with W dequantized as above.
  *   x : device, bf16, row-major [M, K], 16-byte aligned.
  *   W : device, packed buffer of exactly q4_packed_bytes(N, K) bytes, 16-byte aligned.
- *   M : 1..16 verify rows.   N : >= 1 outputs.   K : positive multiple of 64.
+ *   M : 1..32 verify rows (the pages' kernels exist for 8, 16, 24 and 32 rows:
+ *       up to four lanes of eight; "Splash engine", section "The engine
+ *       hard-codes the model").   N : >= 1 outputs.   K : positive multiple of 64.
  *   y : device, fp32, row-major [M, N], 16-byte aligned; fully overwritten.
+ * Row invariance: row m of y is bit-identical for every M (1..32) and every
+ * other row's contents.
  * Device memory: the first call on each device (with that device current)
  * allocates the library's scratch -- split-K partial sums, per-tile counters
  * and the prepared x records, about 14 MB on a 152-SM GPU -- and keeps it
@@ -89,8 +93,9 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
  * that runs inside a host application owning the device allocator, or a
  * latency-critical loop that cannot afford cudaMalloc's implicit device
  * synchronisation.
- *   Arguments, layout, result and accuracy are those of q4_matmul; the
- *   caller still owns x, W and y.  K is limited to 20480 and the device to
+ *   Arguments, layout, result and accuracy are those of q4_matmul, except
+ *   that M is limited to 1..16; the caller still owns x, W and y.  K is
+ *   limited to 20480 and the device to
  *   160 SMs (larger: Q4_ERR_UNSUPPORTED_SHAPE / Q4_ERR_UNSUPPORTED_DEVICE,
  *   nothing launched).
  *   Scratch: a fixed array inside the library's device image (about 8.2 MB),
@@ -165,7 +170,7 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
  * up to top-32": the target's probabilities are the temperature softmax over
  * its first top_k entries, truncated by top_p, renormalized; top_k <= 32).
  *   logits : device, fp32 [M, N] row-major (e.g. the y of the LM-head matmul).
- *   M : 1..16.  N : top_k .. 1,048,576.  top_k : 1..32.  temperature > 0.
+ *   M : 1..32.  N : top_k .. 1,048,576.  top_k : 1..32.  temperature > 0.
  *   top_p > 0 (>= 1 keeps all top_k entries).
  *   idx   : device, int32 [M, 32]: the top_k entries of each row by logit,
  *           largest first, equal logits by lower index first (so the result is

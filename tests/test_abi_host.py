@@ -51,7 +51,7 @@ def test_status_strings():
     ((16, 0, 1, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),        # null W
     ((16, 16, 1, 256, 512, 0), q4.Q4_ERR_INVALID_ARG),        # null y
     ((16, 16, 0, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),       # M = 0
-    ((16, 16, 17, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),      # M = 17
+    ((16, 16, 33, 256, 512, 16), q4.Q4_ERR_INVALID_ARG),      # M = 33
     ((16, 16, 1, 0, 512, 16), q4.Q4_ERR_INVALID_ARG),         # N = 0
     ((16, 16, 1, 256, 96, 16), q4.Q4_ERR_UNSUPPORTED_SHAPE),  # K % 64 != 0
     ((16, 16, 1, 256, 0, 16), q4.Q4_ERR_UNSUPPORTED_SHAPE),   # K = 0
@@ -83,7 +83,7 @@ def test_decode_workspace_size():
     assert need == 16 * 2048 * 4 + 16 * 1024 * 2
     assert lib.q4_decode_step_workspace_bytes(ctypes.addressof(arr), 1, 16) == 0
     assert lib.q4_decode_step_workspace_bytes(None, 3, 16) == 0
-    assert lib.q4_decode_step_workspace_bytes(ctypes.addressof(arr), 3, 17) == 0
+    assert lib.q4_decode_step_workspace_bytes(ctypes.addressof(arr), 3, 33) == 0
 
 
 @pytest.mark.parametrize("spec,ws,status", [
@@ -134,7 +134,7 @@ def test_wait_check_rejects_bad_limits(limit):
 
 @pytest.mark.parametrize("M,N,k,T,p,align,status", [
     (0, 100, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
-    (17, 100, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
+    (33, 100, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
     (2, 100, 0, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
     (2, 100, 33, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
     (2, 5, 8, 1.0, 1.0, 0, q4.Q4_ERR_INVALID_ARG),
@@ -176,3 +176,9 @@ def test_status_names_cover_every_code():
     for code in range(0, 9):
         assert lib.q4_status_string(code).decode().startswith("Q4_")
         assert lib.q4_status_string(code).decode() != "Q4_ERR_UNKNOWN"
+
+
+def test_noalloc_rejects_more_than_16_rows():
+    lib = q4.lib()
+    rc = lib.q4_matmul_noalloc(16, 16, 17, 256, 512, 16, None)
+    assert rc == q4.Q4_ERR_INVALID_ARG, (rc, lib.q4_last_error())

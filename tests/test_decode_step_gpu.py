@@ -105,7 +105,7 @@ def _small_chain(device="cuda"):
     return [(si.make_weights(N, K, 900 + i, device=device), N, K, g) for i, (N, K, g) in enumerate(spec)]
 
 
-@pytest.mark.parametrize("M", [1, 3, 16])
+@pytest.mark.parametrize("M", [1, 3, 16, 24, 32])
 def test_small_chain_teacher_forced(M):
     layers = _small_chain()
     x0 = si.make_x(M, 512, 950 + M, device="cuda")
@@ -117,11 +117,11 @@ def test_small_chain_teacher_forced(M):
 
 def test_small_chain_rows_independent_of_M():
     layers = _small_chain()
-    x16 = si.make_x(16, 512, 960, device="cuda")
-    y16 = q4.decode_step(layers, x16).cpu()
-    for M in (1, 2, 5, 8):
-        yM = q4.decode_step(layers, x16[:M].contiguous()).cpu()
-        assert torch.equal(yM, y16[:M]), f"M={M}"
+    x32 = si.make_x(32, 512, 960, device="cuda")
+    y32 = q4.decode_step(layers, x32).cpu()
+    for M in (1, 2, 5, 8, 16, 17, 24):
+        yM = q4.decode_step(layers, x32[:M].contiguous()).cpu()
+        assert torch.equal(yM, y32[:M]), f"M={M}"
 
 
 def test_decode_step_repeat_is_deterministic():

@@ -28,7 +28,7 @@ def test_tiny_workload_all_rows():
     run_and_check(x, W, N, K, what="tiny")
 
 
-@pytest.mark.parametrize("M", list(range(1, 17)))
+@pytest.mark.parametrize("M", list(range(1, 33)))
 def test_tiny_shape_every_M(M):
     N, K = si.SHAPES["tiny"]
     W = si.make_weights(N, K, 7)
@@ -38,7 +38,8 @@ def test_tiny_shape_every_M(M):
 
 @pytest.mark.parametrize("N,K,M", [(1, 64, 1), (7, 64, 3), (33, 192, 16), (129, 576, 5), (1000, 1024, 16),
                                    (300, 2112, 2), (2, 4160, 9), (517, 5120, 16), (160, 4096, 8),
-                                   (130, 17408, 16)])
+                                   (130, 17408, 16), (33, 192, 24), (517, 5120, 32), (130, 17408, 25),
+                                   (1000, 1024, 17), (300, 2112, 31)])
 def test_ragged_shapes(N, K, M):
     """Ragged N (tails of every tile size), small and odd K, and K spanning
     several shared-memory chunks."""
@@ -47,8 +48,8 @@ def test_ragged_shapes(N, K, M):
     run_and_check(x, W, N, K, what=f"N={N} K={K} M={M}")
 
 
-@pytest.mark.parametrize("name,Ms", [("attn_in", [1, 2, 4, 8, 16]), ("gate_up", [1, 16]), ("down", [1, 16]),
-                                     ("gdn_in", [1, 16]), ("gdn_out", [1, 16])])
+@pytest.mark.parametrize("name,Ms", [("attn_in", [1, 2, 4, 8, 16, 24, 32]), ("gate_up", [1, 16, 32]),
+                                     ("down", [1, 16, 32]), ("gdn_in", [1, 16, 24]), ("gdn_out", [1, 16, 32])])
 def test_model_shapes_sampled(name, Ms):
     """The 27B-shaped projections at full size; sampled columns against the oracle."""
     N, K = si.SHAPES[name]

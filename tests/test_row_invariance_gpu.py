@@ -27,20 +27,24 @@ def _y(x, W, N, K):
 def test_rows_identical_across_M(name):
     N, K = si.SHAPES[name]
     W = si.make_weights(N, K, 5, device="cuda")
-    x16 = si.make_x(16, K, 6, device="cuda")
-    y16 = _y(x16, W, N, K)
-    for M in range(1, 16):
-        yM = _y(x16[:M], W, N, K)
-        assert np.array_equal(yM, y16[:M]), f"M={M}"
+    # 32 rows: both record widths (16 rows for M <= 16, 32 rows above) must give the same bits
+    x32 = si.make_x(32, K, 6, device="cuda")
+    y32 = _y(x32, W, N, K)
+    for M in range(1, 32):
+        yM = _y(x32[:M], W, N, K)
+        assert np.array_equal(yM, y32[:M]), f"M={M}"
     # each row alone, in every position, with other neighbours
-    other = si.make_x(16, K, 9, device="cuda")
-    for m in (0, 5, 15):
-        alone = _y(x16[m:m + 1], W, N, K)
-        assert np.array_equal(alone[0], y16[m])
+    other = si.make_x(32, K, 9, device="cuda")
+    for m in (0, 5, 15, 16, 31):
+        alone = _y(x32[m:m + 1], W, N, K)
+        assert np.array_equal(alone[0], y32[m])
         mixed = other.clone()
-        mixed[15 - m] = x16[m]
+        mixed[31 - m] = x32[m]
         ym = _y(mixed, W, N, K)
-        assert np.array_equal(ym[15 - m], y16[m])
+        assert np.array_equal(ym[31 - m], y32[m])
+        ym16 = _y(mixed[16:].contiguous(), W, N, K)          # the same row in a 16-row call
+        if 31 - m >= 16:
+            assert np.array_equal(ym16[15 - m], y32[m])
 
 
 def test_run_to_run_determinism():

@@ -49,7 +49,7 @@ def _check(y, k, temp, p):
     assert np.all(np.abs(got - ref_p) <= 2.0 * np.spacing(np.float32(np.maximum(ref_p, 1e-38))) + 1e-45)
 
 
-@pytest.mark.parametrize("M", [1, 3, 16])
+@pytest.mark.parametrize("M", [1, 3, 16, 32])
 @pytest.mark.parametrize("k,temp,p", [(32, 1.0, 1.0), (20, 0.7, 0.95), (1, 1.0, 1.0), (8, 2.5, 0.5)])
 def test_lm_head_rows_against_oracle(M, k, temp, p):
     _check(_logits(M, VOCAB, 100 + M + k), k, temp, p)
