@@ -8,7 +8,7 @@ graph and replayed.  value = algorithmic HBM bytes of the step / device time,
 bytes per call = N*K*0.5625 + M*K*2 + M*N*4 (weights once, x once, y once).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload attn_sweep|lm_head|mlp_gdn|full_pass|draft_edges]
+                    [--workload attn_sweep|attn_wide|lm_head|mlp_gdn|full_pass|draft_edges]
 
 full_pass: one step = the whole 27B-shaped verify pass through q4_decode_step
 (64 layers x [in-proj, out-proj, gate/up, down] + the LM head twice, M = 16,
@@ -49,7 +49,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["attn_sweep", "lm_head", "mlp_gdn", "full_pass", "draft_edges"], default="attn_sweep")
+    p.add_argument("--workload", choices=["attn_sweep", "attn_wide", "lm_head", "mlp_gdn", "full_pass", "draft_edges"], default="attn_sweep")
     p.add_argument("--reps", type=int, default=20, help="calls per M per step")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -62,6 +62,10 @@ def workload_spec(name):
     if name == "attn_sweep":
         N, K = si.SHAPES["attn_in"]
         return [("attn_in", N, K, [1, 2, 4, 8, 16])], "attention input projection K=5120->N=14336, M sweep 1,2,4,8,16"
+    if name == "attn_wide":
+        N, K = si.SHAPES["attn_in"]
+        return [("attn_in", N, K, [1, 8, 16, 24, 32])], ("attention input projection K=5120->N=14336, "
+                                                          "M = 1, 8, 16, 24, 32 (up to four lanes of eight rows)")
     if name == "lm_head":
         N, K = si.SHAPES["lm_head"]
         return [("lm_head", N, K, [16, 16])], "LM head K=5120->N=248320, M=16, twice per step"
@@ -107,12 +111,19 @@ def read_peaks():
 
 
 def kernel_source_hash():
-    h = hashlib.sha256()
+    """Hash of what the dominant kernel is made of: its header, the PTX wrappers
+    it uses and the host function that launches it (box, grid, split)."""
     csrc = os.path.join(ROOT, "bit_row_speculative_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    h = hashlib.sha256()
+    for fn in ("q4_tm.cuh", "q4_sm100.cuh"):
         with open(os.path.join(csrc, fn), "rb") as fh:
             h.update(fn.encode())
             h.update(fh.read())
+    with open(os.path.join(csrc, "q4_abi.cu")) as fh:
+        abi = fh.read()
+    i = abi.find("q4_status launch_tm(")
+    j = abi.find("\n}\n", i)
+    h.update(abi[i:j].encode() if i >= 0 and j > i else abi.encode())
     return h.hexdigest()[:16]
 
 
@@ -377,9 +388,11 @@ def run_ours(args, rank, world, local_rank):
         us = per_graph_ms[i] / (args.steps * args.reps) * 1e3
         per_m[f"{label}_M{M}"] = {"us_per_call": round(us, 3),
                                   "GBs": round(call_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
-    ratio = None
-    if args.workload == "attn_sweep":
+    ratio = ratio32 = None
+    if args.workload in ("attn_sweep", "attn_wide"):
         ratio = per_m["attn_in_M16"]["us_per_call"] / per_m["attn_in_M1"]["us_per_call"]
+    if args.workload == "attn_wide":
+        ratio32 = per_m["attn_in_M32"]["us_per_call"] / per_m["attn_in_M1"]["us_per_call"]
 
     # LM head: the sampling epilogue (top-32, temperature 1, top_p 0.95) on the
     # head's own logits; bytes = the logits read once + the 32 (index, prob) pairs per row
@@ -453,6 +466,7 @@ def run_ours(args, rank, world, local_rank):
                          f"({l2 / 2**20:.0f} MiB); one CUDA graph per M",
                    "parallelism": f"replicas x{world}"},
         "per_M": per_m, "ratio_M16_over_M1": None if ratio is None else round(ratio, 4),
+        "ratio_M32_over_M1": None if ratio32 is None else round(ratio32, 4),
         "sampling_epilogue": epilogue,
         "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
