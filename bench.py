@@ -285,6 +285,86 @@ def run_reference_edges(args, world):
     print(json.dumps(line), flush=True)
 
 
+def e2e_pipelined(args, spec, pools, xs, ys, stream, dev, world, step_bytes, chunk=10):
+    """End to end through q4.matmul with host buffers.  Every call of a step
+    copies its own x from pinned host memory to the device and reads its own y
+    back to pinned host memory.  The copies run on a second stream, a chunk of
+    calls at a time: the inputs of chunk j + 1 are copied and the results of
+    chunk j - 1 read back while chunk j's matmuls run, and the matmul stream
+    waits once per chunk (so consecutive matmuls stay chained).  The step,
+    copies included, is captured once in a CUDA graph and replayed, as a
+    serving loop would."""
+    import torch
+    import bit_row_speculative_gb300 as q4
+    calls = [(label, N, K, M, r) for label, N, K, Ms in spec for M in Ms for r in range(args.reps)]
+    hx = [xs[(c[0], c[3])].cpu().pin_memory() for c in calls]
+    hy = [torch.empty(ys[(c[0], c[3])].shape, dtype=torch.float32).pin_memory() for c in calls]
+    dx = [torch.empty_like(xs[(c[0], c[3])]) for c in calls]
+    dy = [torch.empty_like(ys[(c[0], c[3])]) for c in calls]
+    h2d = sum(t.numel() * 2 for t in hx)
+    d2h = sum(t.numel() * 4 for t in hy)
+    cs = torch.cuda.Stream(device=dev)
+    chunks = [list(range(a, min(a + chunk, len(calls)))) for a in range(0, len(calls), chunk)]
+
+    def step():
+        ev_in = [torch.cuda.Event() for _ in chunks]
+        ev_mm = [torch.cuda.Event() for _ in chunks]
+
+        def copy_in(j):
+            with torch.cuda.stream(cs):
+                for k in chunks[j]:
+                    dx[k].copy_(hx[k], non_blocking=True)
+                ev_in[j].record(cs)
+
+        def read_back(j):
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_mm[j])
+                for k in chunks[j]:
+                    hy[k].copy_(dy[k], non_blocking=True)
+
+        cs.wait_stream(stream)
+        copy_in(0)
+        for j, ks in enumerate(chunks):
+            if j + 1 < len(chunks):
+                copy_in(j + 1)
+            stream.wait_event(ev_in[j])
+            for k in ks:
+                label, N, K, M, r = calls[k]
+                W = pools[label][(r * 5 + M) % len(pools[label])]
+                q4.matmul(dx[k], W, N, K, y=dy[k], stream=stream)
+            ev_mm[j].record(stream)
+            read_back(j)
+        stream.wait_stream(cs)
+
+    how = "graph"
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        run = g.replay
+    except Exception as exc:                             # report, then measure eagerly
+        how = f"eager ({type(exc).__name__} in capture)"
+        run = step
+    with torch.cuda.stream(stream):
+        run()
+    stream.synchronize()
+    e_steps = max(1, min(args.steps, 5))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            run()
+        e1.record(stream)
+    stream.synchronize()
+    q4.device_status(stream)
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+    return {"value": round(job_throughput(step_bytes, 1, e_ms, world), 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
+            "how": f"{how}: every call's x copied from pinned host memory and its y read back to pinned host "
+                   f"memory, on a second stream in chunks of {chunk} calls overlapping the matmuls"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import bit_row_speculative_gb300 as q4
@@ -422,33 +502,7 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through the public API with host buffers: per call, pinned
     # host x -> device, the matmul, device y -> pinned host
-    e2e = None
-    if True:
-        hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
-        hy = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in ys.items()}
-        dx = {k: torch.empty_like(v) for k, v in xs.items()}
-        h2d = sum(hx[(label, M)].numel() * 2 for label, N, K, Ms in spec for M in Ms) * args.reps
-        d2h = sum(hy[(label, M)].numel() * 4 for label, N, K, Ms in spec for M in Ms) * args.reps
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e_steps = max(1, min(args.steps, 5))
-        with torch.cuda.stream(stream):
-            for s in range(e_steps + 1):
-                if s == 1:
-                    e0.record(stream)
-                for label, N, K, Ms in spec:
-                    for M in Ms:
-                        for r in range(args.reps):
-                            dx[(label, M)].copy_(hx[(label, M)], non_blocking=True)
-                            W = pools[label][(r * 5 + M) % len(pools[label])]
-                            q4.matmul(dx[(label, M)], W, N, K, y=ys[(label, M)])
-                            hy[(label, M)].copy_(ys[(label, M)], non_blocking=True)
-            e1.record(stream)
-        stream.synchronize()
-        e_ms = e0.elapsed_time(e1) / e_steps
-        e_ms = max_over_ranks(e_ms, world, dev)
-        e2e = {"value": round(job_throughput(step_bytes, 1, e_ms, world), 1), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+    e2e = e2e_pipelined(args, spec, pools, xs, ys, stream, dev, world, step_bytes)
 
     if rank != 0:
         return
@@ -687,30 +741,71 @@ def run_edges(args, rank, world, local_rank):
     kernel_ms = max_over_ranks(sum(call_ms), world, dev)
     value = job_throughput(call_b * args.reps, args.steps, kernel_ms, world)
 
-    # end to end through the public call: pinned host hidden and ids -> device,
-    # the call, scores -> pinned host, every call
-    hh = [tuple(t.pin_memory() for t in inp) for inp in host_inputs]
-    hs = torch.empty(score.shape, dtype=score.dtype).pin_memory()
-    dh, dp, dc = (torch.empty_like(t) for t in dev_inputs[0])
-    e_calls = 50
+    # end to end through the public call: every call copies its hidden and ids
+    # from pinned host memory and reads its scores back, on a second stream in
+    # chunks of 10 calls overlapping the kernels; captured once in a CUDA graph
+    n_e = 50
+    hh = [tuple(t.pin_memory() for t in host_inputs[k % len(host_inputs)]) for k in range(n_e)]
+    dd = [tuple(torch.empty_like(t, device=dev) for t in hh[k]) for k in range(n_e)]
+    hs = [torch.empty(score.shape, dtype=score.dtype).pin_memory() for _ in range(n_e)]
+    ds = [torch.empty_like(score) for _ in range(n_e)]
+    cs = torch.cuda.Stream(device=dev)
+    chunks = [list(range(a, min(a + 10, n_e))) for a in range(0, n_e, 10)]
+
+    def e2e_step():
+        ev_in = [torch.cuda.Event() for _ in chunks]
+        ev_k = [torch.cuda.Event() for _ in chunks]
+
+        def copy_in(j):
+            with torch.cuda.stream(cs):
+                for k in chunks[j]:
+                    for d_, h_ in zip(dd[k], hh[k]):
+                        d_.copy_(h_, non_blocking=True)
+                ev_in[j].record(cs)
+
+        cs.wait_stream(stream)
+        copy_in(0)
+        for j, ks in enumerate(chunks):
+            if j + 1 < len(chunks):
+                copy_in(j + 1)
+            stream.wait_event(ev_in[j])
+            for k in ks:
+                q4.draft_select_edges(P, S, dd[k][0], dd[k][1], dd[k][2], score=ds[k], stream=stream)
+            ev_k[j].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_k[j])
+                for k in ks:
+                    hs[k].copy_(ds[k], non_blocking=True)
+        stream.wait_stream(cs)
+
+    how = "graph"
+    ge = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(ge, stream=stream):
+            e2e_step()
+        run = ge.replay
+    except Exception as exc:
+        how = f"eager ({type(exc).__name__} in capture)"
+        run = e2e_step
+    with torch.cuda.stream(stream):
+        run()
+    stream.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for k in range(e_calls + 1):
-            if k == 1:
-                e0.record(stream)
-            h, pr, ca = hh[k % len(hh)]
-            dh.copy_(h, non_blocking=True)
-            dp.copy_(pr, non_blocking=True)
-            dc.copy_(ca, non_blocking=True)
-            q4.draft_select_edges(P, S, dh, dp, dc, score=score, stream=stream)
-            hs.copy_(score, non_blocking=True)
+        e0.record(stream)
+        for _ in range(3):
+            run()
         e1.record(stream)
     stream.synchronize()
-    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_calls, world, dev)
+    q4.device_status(stream)
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / (3 * n_e), world, dev)
+    per_call_in = sum(t.numel() * t.element_size() for t in hh[0])
     e2e = {"value": round(job_throughput(call_b, 1, e_ms, world), 2), "unit": "GB/s",
-           "h2d_bytes_per_step": (dh.numel() * 4 + dp.numel() * 4 + dc.numel() * 4) * args.reps,
-           "d2h_bytes_per_step": hs.numel() * 4 * args.reps, "us_per_call": round(e_ms * 1e3, 3)}
+           "h2d_bytes_per_step": per_call_in * args.reps, "d2h_bytes_per_step": hs[0].numel() * 4 * args.reps,
+           "us_per_call": round(e_ms * 1e3, 3),
+           "how": f"{how}: every call's hidden and ids copied in and its scores read back, on a second stream in "
+                  "chunks of 10 calls overlapping the kernels"}
 
     if rank != 0:
         return
