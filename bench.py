@@ -644,7 +644,8 @@ def run_full_pass(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
                      "algorithmic_bytes_per_launch": step_bytes // n_mm,
                      "note": "whole step (matmul and glue launches) timed; a lower bound for the matmul kernel"},
-        "gpu_launches": (2 * n_mm + (n_mm - 1)) * args.steps,   # x records + matmul per layer, glue between
+        # matmul per layer, glue between (writing the next layer's x records), x records for layer 0
+        "gpu_launches": (n_mm + (n_mm - 1) + 1) * args.steps,
         "clocks": clocks, "e2e": e2e,
     }
     if not args.no_cpu_baseline:

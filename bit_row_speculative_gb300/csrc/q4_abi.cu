@@ -293,7 +293,7 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
 }
 
 q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, bool records_ready) {
     using namespace q4::tm;
     CUtensorMap map_nib;
     q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
@@ -318,10 +318,12 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
     p.trace = g_trace;
 #endif
     const int MT = tm_rows_template(M);
-    cudaError_t e = MT <= 16 ? launch_pdl(xrec_kernel<16>, dim3((unsigned)p.G), dim3(8 * 16), 0, stream,
-                                          static_cast<const uint16_t*>(x), M, K, d.xt)
-                             : launch_pdl(xrec_kernel<32>, dim3((unsigned)p.G), dim3(8 * 32), 0, stream,
-                                          static_cast<const uint16_t*>(x), M, K, d.xt);
+    cudaError_t e = cudaSuccess;
+    if (!records_ready)   // else the preceding glue kernel wrote them
+        e = MT <= 16 ? launch_pdl(xrec_kernel<16>, dim3((unsigned)p.G), dim3(8 * 16), 0, stream,
+                                  static_cast<const uint16_t*>(x), M, K, d.xt)
+                     : launch_pdl(xrec_kernel<32>, dim3((unsigned)p.G), dim3(8 * 32), 0, stream,
+                                  static_cast<const uint16_t*>(x), M, K, d.xt);
     if (e != cudaSuccess) return cuda_fail(e, "launching the x record kernel");
     const dim3 grid((unsigned)p.C), block(kThreads);
     switch (MT) {
@@ -382,17 +384,25 @@ bool use_tc(int64_t N, int64_t K) {
 
 // The kernel for a (validated) matmul: the tensor-memory kernel for K a
 // multiple of 512, the generic kernel otherwise.
+// developer comparison switch: 1 = two-launch tensor-memory kernel, 2 = register-operand kernel
+int alt_kernel_choice() {
+    static const int alt = [] {
+        const char* v = std::getenv("Q4_ALT_KERNEL");
+        return v ? std::atoi(v) : 0;
+    }();
+    return alt;
+}
+
+// records_ready: the x records of this call are already in the scratch (written by
+// a glue kernel in record mode); only valid when use_tc(N, K).
 q4_status dispatch_matmul(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool records_ready = false) {
+    if (records_ready) return launch_tm(d, x, W, M, N, K, y, stream, true);
     if (use_tc(N, K)) {
-        // developer comparison switch: 1 = two-launch tensor-memory kernel, 2 = register-operand kernel
-        static const int alt_kernel = [] {
-            const char* v = std::getenv("Q4_ALT_KERNEL");
-            return v ? std::atoi(v) : 0;
-        }();
+        const int alt_kernel = alt_kernel_choice();
         if (alt_kernel == 1 && M <= 16) return launch_tc(d, x, W, M, N, K, y, stream);
         if (alt_kernel == 2 && M <= 16) return launch_rk(d, x, W, M, N, K, y, stream);
-        return launch_tm(d, x, W, M, N, K, y, stream);
+        return launch_tm(d, x, W, M, N, K, y, stream, false);
     }
     return launch_generic(x, W, M, N, K, y, stream);
 }
@@ -437,7 +447,10 @@ q4_status check_glue_args(const float* y, int M, int64_t n_prev, int64_t K, int 
 }
 
 // One cluster of glue::slices(K) CTAs per row, chained by programmatic dependent launch.
-q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind, void* x, cudaStream_t stream) {
+// x mode (rec == nullptr): x_next bf16 [M, K] to x.  Record mode: the next
+// matmul's x records (row width rec_w) to rec instead.
+q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind, void* x, cudaStream_t stream,
+                      uint8_t* rec = nullptr, int rec_w = 16) {
     const int S = q4::glue::slices(K);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S, (unsigned)M);
@@ -454,7 +467,7 @@ q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, q4::glue::glue_kernel, y, n_prev, K, kind, kGlueEps,
-                                       static_cast<uint16_t*>(x));
+                                       static_cast<uint16_t*>(x), rec, rec_w);
     if (e != cudaSuccess) return cuda_fail(e, "launching the glue kernel");
     return Q4_OK;
 }
@@ -702,14 +715,19 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
     float* ybuf = static_cast<float*>(workspace);
     void* xbuf = static_cast<uint8_t*>(workspace) + yb;
     const void* xj = x0;
+    bool records_ready = false;
+    const int rec_w = tm_rows_template(M) > 16 ? 32 : 16;
     for (int j = 0; j < n_layers; ++j) {
         const q4_layer& L = layers[j];
         const bool last = j + 1 == n_layers;
         float* yj = last ? y_last : ybuf;
-        s = dispatch_matmul(*info, xj, L.W, M, L.N, L.K, yj, st);
+        s = dispatch_matmul(*info, xj, L.W, M, L.N, L.K, yj, st, records_ready);
         if (s != Q4_OK) return s;
         if (!last) {
-            s = launch_glue(yj, M, L.N, layers[j + 1].K, L.glue, xbuf, st);
+            const q4_layer& Nx = layers[j + 1];
+            // the next matmul on the tensor-memory kernel: the glue writes its x records directly
+            records_ready = use_tc(Nx.N, Nx.K) && alt_kernel_choice() == 0;
+            s = launch_glue(yj, M, L.N, Nx.K, L.glue, xbuf, st, records_ready ? info->xt : nullptr, rec_w);
             if (s != Q4_OK) return s;
             xj = xbuf;
         }

@@ -10,8 +10,15 @@
 // values of a long chain of linears in range.
 //
 // Work split: one thread-block cluster per row, S = slices(K) CTAs (at most 8)
-// each owning a contiguous slice of the row, so a step's glue runs on up to
-// 8*M SMs instead of M.  S depends on K only.
+// each owning a contiguous slice of the row made of whole groups of 64 inputs,
+// so a step's glue runs on up to 8*M SMs instead of M.  S and the slices
+// depend on K only.
+//
+// Two outputs.  x mode writes x_next as bf16 [M, K].  Record mode (inside a
+// chained pass, when the next matmul runs the tensor-memory kernel) writes the
+// next matmul's x records instead -- the same bf16 values, permuted and scaled
+// into the record layout, and the group sums X added in the record kernel's
+// order -- so that matmul needs no record kernel and x_next is never stored.
 //
 // Arithmetic: the definition is evaluated as if in double, at single-precision
 // cost.  The sum of squares is kept as an unevaluated pair of floats (each
@@ -33,6 +40,8 @@
 #include <cstdint>
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
+
+#include "q4_tm.cuh"
 
 namespace q4 {
 namespace glue {
@@ -61,6 +70,21 @@ __device__ __forceinline__ double value_d(const float* yr, int64_t K, int64_t k,
     return a;
 }
 
+// One output x[m, k] as bf16 bits: computed in float and rounded, unless it lies
+// within kTieMargin float ulps of a bf16 rounding midpoint, where it is
+// recomputed in double and rounded from there.
+__device__ __forceinline__ uint16_t output_bits(const float* yr, int64_t K, int64_t k, int kind, double inv,
+                                                float inv_f) {
+    const float t = __fmul_rn(value_f(yr, K, k, kind), inv_f);
+    const int low = (int)(__float_as_uint(t) & 0xFFFFu);
+    __nv_bfloat16 h;
+    if (abs(low - 0x8000) <= kTieMargin)
+        h = __double2bfloat16(value_d(yr, K, k, kind) * inv);   // near a tie: decide in double
+    else
+        h = __float2bfloat16_rn(t);
+    return *reinterpret_cast<const uint16_t*>(&h);
+}
+
 // (hi, lo) += (p, e) with an error-free two-sum of the high parts.
 __device__ __forceinline__ void ff_add(float& hi, float& lo, float p, float e) {
     const float t = __fadd_rn(hi, p);
@@ -71,8 +95,10 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float p, float e) {
 }
 
 // grid (S, M), cluster (S, 1, 1): CTA (s, m) owns inputs [s*L, min(K, (s+1)*L)) of row m.
+// x: bf16 [M, K] (x mode) or nullptr; rec: the next matmul's records [K/64][rec_bytes(rec_w)] (record mode) or nullptr.
 __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict__ y, int64_t n_prev, int64_t K,
-                                                        int kind, double eps, uint16_t* __restrict__ x) {
+                                                        int kind, double eps, uint16_t* __restrict__ x,
+                                                        uint8_t* __restrict__ rec, int rec_w) {
     namespace cg = cooperative_groups;
     __shared__ float part_hi[kThreads / 32], part_lo[kThreads / 32];
     __shared__ float slice_sum[2];
@@ -82,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     const int S = (int)gridDim.x;
     const int s = (int)blockIdx.x;
     const int m = (int)blockIdx.y;
-    const int64_t L = (K + S - 1) / S;
+    const int64_t L = (K / 64 + S - 1) / S * 64;     // whole groups
     const int64_t k0 = (int64_t)s * L;
     const int64_t k1 = (k0 + L < K) ? k0 + L : K;
     const float* yr = y + (int64_t)m * n_prev;
@@ -135,16 +161,43 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     cluster.sync();                                   // no CTA leaves while another still reads its sum
     const double inv = inv_s;
     const float inv_f = (float)inv;
-    uint16_t* xr = x + (int64_t)m * K;
-    for (int64_t kk = k0 + threadIdx.x; kk < k1; kk += kThreads) {
-        const float t = __fmul_rn(value_f(yr, K, kk, kind), inv_f);
-        const int low = (int)(__float_as_uint(t) & 0xFFFFu);
-        __nv_bfloat16 h;
-        if (abs(low - 0x8000) <= kTieMargin)
-            h = __double2bfloat16(value_d(yr, K, kk, kind) * inv);   // near a tie: decide in double
-        else
-            h = __float2bfloat16_rn(t);
-        xr[kk] = *reinterpret_cast<const uint16_t*>(&h);
+    if (rec == nullptr) {
+        uint16_t* xr = x + (int64_t)m * K;
+        for (int64_t kk = k0 + threadIdx.x; kk < k1; kk += kThreads) xr[kk] = output_bits(yr, K, kk, kind, inv, inv_f);
+        return;
+    }
+    // record mode: thread b takes the 8-block of inputs k0 + 8b .. k0 + 8b + 7; the
+    // 8 blocks of a group sit in 8 consecutive lanes (slices are whole groups)
+    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8;
+    const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
+    for (int64_t b0 = 0; b0 < nblk; b0 += kThreads) {      // uniform over the CTA: whole warps take part
+        const int64_t b = b0 + threadIdx.x;
+        const bool active = b < nblk;
+        uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (active) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[e] = output_bits(yr, K, k0 + 8 * b + e, kind, inv, inv_f);
+        }
+        // the group sum X: the 8 values in increasing k, then the 8 blocks by a fixed xor tree
+        float sx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sx = __fadd_rn(sx, __uint_as_float(h[e] << 16));
+        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 1));
+        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 2));
+        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 4));
+        if (active) {
+            const int64_t kb = k0 + 8 * b;                    // first input of the block
+            const int64_t g = kb / 64;
+            const int kc = (int)((kb / 8) & 7);
+            uint8_t* r = rec + g * rb;
+            uint4 o;                                          // pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), scaled
+            o.x = q4::tm::bf16x2_mul(h[0] | (h[4] << 16), q4::tm::kXScaleEven);
+            o.y = q4::tm::bf16x2_mul(h[1] | (h[5] << 16), q4::tm::kXScaleOdd);
+            o.z = q4::tm::bf16x2_mul(h[2] | (h[6] << 16), q4::tm::kXScaleEven);
+            o.w = q4::tm::bf16x2_mul(h[3] | (h[7] << 16), q4::tm::kXScaleOdd);
+            *reinterpret_cast<uint4*>(r + rb0 + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
+            if (kc == 0) reinterpret_cast<float*>(r)[m] = sx;
+        }
     }
 }
 
