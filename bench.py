@@ -499,6 +499,26 @@ def run_ours(args, rank, world, local_rank):
         epilogue = {"what": "q4_topk_probs top_k=32 T=1 top_p=0.95 on the head's logits", "M": yl.shape[0],
                     "us_per_call": round(us, 3), "GBs": round(ebytes / (us * 1e-6) / 1e9, 1),
                     "launches_per_call": 1}
+        # the head and its epilogue fused (q4_lm_head_topk: logits in the library's scratch,
+        # dropped from L2 after the epilogue reads them)
+        xl = xs[(label, Ms[0])]
+        with torch.cuda.stream(stream):
+            for k in range(3):
+                q4.lm_head_topk(xl, pools[label][k % len(pools[label])], N, K, 32, 1.0, 0.95, idx=ei, probs=ep,
+                                stream=stream)
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            freps = 10
+            f0.record(stream)
+            for k in range(freps):
+                q4.lm_head_topk(xl, pools[label][k % len(pools[label])], N, K, 32, 1.0, 0.95, idx=ei, probs=ep,
+                                stream=stream)
+            f1.record(stream)
+        stream.synchronize()
+        q4.device_status(stream)
+        fus = f0.elapsed_time(f1) / freps * 1e3
+        epilogue["fused_head_and_epilogue"] = {"what": "q4_lm_head_topk (matmul + epilogue, logits not stored)",
+                                               "us_per_call": round(fus, 3), "launches_per_call": 3}
 
     # end to end through the public API with host buffers: per call, pinned
     # host x -> device, the matmul, device y -> pinned host

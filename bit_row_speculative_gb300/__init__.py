@@ -30,7 +30,7 @@ GROUP = 64
 
 # Exported symbols (one per function declared in include/q4.h).
 SYMBOLS = ("q4_packed_bytes", "q4_matmul", "q4_matmul_noalloc", "q4_glue", "q4_decode_step_workspace_bytes",
-           "q4_decode_step", "q4_topk_probs", "q4_draft_select_edges", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
+           "q4_decode_step", "q4_topk_probs", "q4_lm_head_topk", "q4_draft_select_edges", "q4_check_wait_timeout", "q4_device_status", "q4_last_error", "q4_status_string")
 
 GLUE_NONE = 0
 GLUE_RMSNORM = 1
@@ -70,6 +70,9 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.q4_topk_probs.restype = c.c_int
     lib.q4_topk_probs.argtypes = [c.c_void_p, c.c_int, c.c_int64, c.c_int, c.c_float, c.c_float, c.c_void_p,
                                   c.c_void_p, c.c_void_p]
+    lib.q4_lm_head_topk.restype = c.c_int
+    lib.q4_lm_head_topk.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int, c.c_float,
+                                    c.c_float, c.c_void_p, c.c_void_p, c.c_void_p]
     lib.q4_draft_select_edges.restype = c.c_int
     lib.q4_draft_select_edges.argtypes = [c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_void_p, c.c_void_p,
                                           c.c_void_p, c.c_int, c.c_void_p, c.c_void_p]
@@ -220,6 +223,23 @@ def topk_probs(logits, top_k: int, temperature: float, top_p: float, idx=None, p
         probs = torch.empty((M, 32), dtype=torch.float32, device=logits.device)
     _check(lib().q4_topk_probs(logits.data_ptr(), M, N, int(top_k), float(temperature), float(top_p),
                                idx.data_ptr(), probs.data_ptr(), _stream_handle(stream)))
+    return idx, probs
+
+
+def lm_head_topk(x, W, N: int, K: int, top_k: int, temperature: float, top_p: float, idx=None, probs=None,
+                 stream=None):
+    """The LM head and its sampling epilogue in one call: (idx int32 [M, 32], probs fp32 [M, 32])
+    for bf16 device x [M, K] and the packed head W; the logits stay in the library's scratch."""
+    import torch
+    M = x.shape[0]
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bfloat16 tensor")
+    if idx is None:
+        idx = torch.empty((M, 32), dtype=torch.int32, device=x.device)
+    if probs is None:
+        probs = torch.empty((M, 32), dtype=torch.float32, device=x.device)
+    _check(lib().q4_lm_head_topk(x.data_ptr(), W.data_ptr(), M, N, K, int(top_k), float(temperature), float(top_p),
+                                 idx.data_ptr(), probs.data_ptr(), _stream_handle(stream)))
     return idx, probs
 
 

@@ -735,13 +735,14 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
     return Q4_OK;
 }
 
-q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float temperature, float top_p,
-                        int32_t* idx, float* probs, q4_stream_t stream) {
-    g_last_error.clear();
+namespace {
+
+// Argument checks of the sampling epilogue (everything but the device and the logits pointer).
+q4_status check_topk_args(int M, int64_t N, int top_k, float temperature, float top_p, const int32_t* idx,
+                          const float* probs) {
     using namespace q4::topk;
-    if (!logits || !idx || !probs)
-        return fail(Q4_ERR_INVALID_ARG, "null pointer argument (logits=%p idx=%p probs=%p)", (const void*)logits,
-                    (void*)idx, (void*)probs);
+    if (!idx || !probs)
+        return fail(Q4_ERR_INVALID_ARG, "null pointer argument (idx=%p probs=%p)", (const void*)idx, (const void*)probs);
     if (M < 1 || M > Q4_MAX_ROWS) return fail(Q4_ERR_INVALID_ARG, "M = %d is outside 1..%d", M, Q4_MAX_ROWS);
     if (top_k < 1 || top_k > kWidth) return fail(Q4_ERR_INVALID_ARG, "top_k = %d is outside 1..%d", top_k, kWidth);
     if (N < top_k) return fail(Q4_ERR_INVALID_ARG, "N = %lld is smaller than top_k = %d", (long long)N, top_k);
@@ -750,19 +751,82 @@ q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float 
     if (!(temperature > 0.0f) || !(temperature < 3.0e38f))
         return fail(Q4_ERR_INVALID_ARG, "temperature must be positive and finite");
     if (!(top_p > 0.0f)) return fail(Q4_ERR_INVALID_ARG, "top_p must be positive");
-    if (!aligned16(logits) || !aligned16(idx) || !aligned16(probs))
-        return fail(Q4_ERR_MISALIGNED, "logits, idx and probs must be 16-byte aligned");
-    int dev = 0;
-    const DeviceInfo* info = nullptr;
-    q4_status s = device_setup(&dev, &info);
-    if (s != Q4_OK) return s;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!aligned16(idx) || !aligned16(probs)) return fail(Q4_ERR_MISALIGNED, "idx and probs must be 16-byte aligned");
+    return Q4_OK;
+}
+
+q4_status launch_topk(const DeviceInfo& d, const float* logits, int M, int64_t N, int top_k, float temperature,
+                      float top_p, int32_t* idx, float* probs, cudaStream_t st, int discard) {
+    using namespace q4::topk;
     const int S = (int)((N + kSlice - 1) / kSlice);
-    const int64_t L = ((N + S - 1) / S + 3) / 4 * 4;          // <= kSlice; slices start 16-byte aligned when N % 4 == 0
+    // <= kSlice; a multiple of 32 floats, so slices start on 128-byte lines when each row does
+    const int64_t L = ((N + S - 1) / S + 31) / 32 * 32;
     const cudaError_t e = launch_pdl(topk_kernel, dim3((unsigned)S, (unsigned)M), dim3(kThreads), 0, st, logits, N, L,
-                                     top_k, temperature, top_p, info->topk_cand, info->topk_tickets, idx, probs);
+                                     top_k, temperature, top_p, d.topk_cand, d.topk_tickets, idx, probs, discard);
     if (e != cudaSuccess) return cuda_fail(e, "launching the top-k kernel");
     return Q4_OK;
+}
+
+// Logits scratch of q4_lm_head_topk, per device, grown on demand.
+struct LogitsScratch {
+    float* ptr = nullptr;
+    size_t bytes = 0;
+};
+LogitsScratch g_logits[kMaxDevices];
+std::mutex g_logits_mutex;
+
+}  // namespace
+
+q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float temperature, float top_p,
+                        int32_t* idx, float* probs, q4_stream_t stream) {
+    g_last_error.clear();
+    if (!logits) return fail(Q4_ERR_INVALID_ARG, "null pointer argument (logits)");
+    q4_status s = check_topk_args(M, N, top_k, temperature, top_p, idx, probs);
+    if (s != Q4_OK) return s;
+    if (!aligned16(logits)) return fail(Q4_ERR_MISALIGNED, "logits, idx and probs must be 16-byte aligned");
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    return launch_topk(*info, logits, M, N, top_k, temperature, top_p, idx, probs,
+                       reinterpret_cast<cudaStream_t>(stream), 0);
+}
+
+q4_status q4_lm_head_topk(const void* x, const void* W, int M, int64_t N, int64_t K, int top_k, float temperature,
+                          float top_p, int32_t* idx, float* probs, q4_stream_t stream) {
+    g_last_error.clear();
+    q4_status s = check_matmul_args(x, W, M, N, K, probs);
+    if (s != Q4_OK) return s;
+    s = check_topk_args(M, N, top_k, temperature, top_p, idx, probs);
+    if (s != Q4_OK) return s;
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    s = device_setup(&dev, &info);
+    if (s != Q4_OK) return s;
+    float* logits = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_logits_mutex);
+        LogitsScratch& ls = g_logits[dev];
+        const size_t need = (size_t)M * (size_t)N * sizeof(float);
+        if (ls.bytes < need) {
+            if (ls.ptr) {
+                cudaError_t e = cudaDeviceSynchronize();   // earlier calls may still use the old buffer
+                if (e == cudaSuccess) e = cudaFree(ls.ptr);
+                if (e != cudaSuccess) return cuda_fail(e, "freeing the logits scratch");
+                ls.ptr = nullptr;
+                ls.bytes = 0;
+            }
+            const size_t grow = (size_t)Q4_MAX_ROWS * (size_t)N * sizeof(float);
+            const cudaError_t e = cudaMalloc(&ls.ptr, grow);
+            if (e != cudaSuccess) return cuda_fail(e, "allocating the logits scratch");
+            ls.bytes = grow;
+        }
+        logits = ls.ptr;
+    }
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    s = dispatch_matmul(*info, x, W, M, N, K, logits, st);
+    if (s != Q4_OK) return s;
+    return launch_topk(*info, logits, M, N, top_k, temperature, top_p, idx, probs, st, 1);
 }
 
 q4_status q4_draft_select_edges(const void* pred_cb, const void* succ_cb, int64_t V, int R, const float* hidden,

@@ -111,10 +111,13 @@ __device__ __forceinline__ void load_run(const float* row, int i, int len, bool 
 
 // cand: [M][S][32] scratch; tickets: [M] counters, zero between launches.
 // idx, probs: [M][32].
+// discard != 0 (logits in the library's own scratch): once the slice is read,
+// its whole 128-byte L2 lines are invalidated without being written back.
 __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restrict__ logits, int64_t N, int64_t L,
                                                         int top_k, float temperature, float top_p,
                                                         uint64_t* __restrict__ cand, int* __restrict__ tickets,
-                                                        int32_t* __restrict__ idx, float* __restrict__ probs) {
+                                                        int32_t* __restrict__ idx, float* __restrict__ probs,
+                                                        int discard) {
     __shared__ uint64_t buf[kCap];
     __shared__ uint64_t lists[kWarps][32];
     __shared__ uint64_t bound;
@@ -169,7 +172,13 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restri
             }
         }
     }
-    __syncthreads();
+    __syncthreads();                                           // every logit of the slice has been read
+    if (discard) {
+        const uintptr_t b0 = (reinterpret_cast<uintptr_t>(row) + 127) & ~uintptr_t(127);
+        const uintptr_t b1 = reinterpret_cast<uintptr_t>(row + len) & ~uintptr_t(127);
+        for (uintptr_t a = b0 + (uintptr_t)tid * 128; a < b1; a += (uintptr_t)kThreads * 128)
+            asm volatile("discard.global.L2 [%0], 128;" ::"l"(a) : "memory");
+    }
 
     // 3. the slice's top 32: warp w sorts chunks w, w + 8, ... of 32 candidates and
     //    keeps the top 32 of them; the warps' lists are then merged by warp 0

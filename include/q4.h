@@ -183,6 +183,23 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
 q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float temperature, float top_p,
                         int32_t* idx, float* probs, q4_stream_t stream);
 
+/* The LM head with its sampling epilogue fused: q4_matmul of x[M,K] against
+ * the packed head W[N,K] into the library's own logits scratch, then the
+ * q4_topk_probs epilogue on those logits ("Splash engine" analysis, section
+ * "Exact, up to top-32": top-32 sampling follows the head in the same step).
+ * The logits never leave the GPU's L2: as each epilogue CTA finishes reading
+ * its slice it invalidates those cache lines without writing them back, so the
+ * M*N*4 bytes of logits are not written to HBM (when they are still resident).
+ *   Arguments and results are those of q4_matmul (x, W, M, N, K) and of
+ *   q4_topk_probs (top_k, temperature, top_p, idx, probs); idx and probs are
+ *   bit-identical to q4_matmul followed by q4_topk_probs.
+ * Device memory: the first call for a given N allocates a logits scratch of
+ * 32*N*4 bytes on the current device (grown, never shrunk, held until exit);
+ * make that call outside any stream capture.  The same scratch rules as
+ * q4_matmul apply to concurrent calls. */
+q4_status q4_lm_head_topk(const void* x, const void* W, int M, int64_t N, int64_t K, int top_k, float temperature,
+                          float top_p, int32_t* idx, float* probs, q4_stream_t stream);
+
 /* Edge scores of the draft selector ("Splash engine" analysis, section "The
  * draft is a small model with an unusual selector": the top 16 candidates of
  * each draft position are scored against 16 predecessors by a trilinear form

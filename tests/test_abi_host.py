@@ -182,3 +182,15 @@ def test_noalloc_rejects_more_than_16_rows():
     lib = q4.lib()
     rc = lib.q4_matmul_noalloc(16, 16, 17, 256, 512, 16, None)
     assert rc == q4.Q4_ERR_INVALID_ARG, (rc, lib.q4_last_error())
+
+
+def test_fused_head_rejects_bad_arguments():
+    lib = q4.lib()
+    ok = (16, 16, 4, 256, 512, 8, 1.0, 1.0, 16, 16, None)
+    assert lib.q4_lm_head_topk(*ok[:2], 33, *ok[3:]) == q4.Q4_ERR_INVALID_ARG            # M = 33
+    assert lib.q4_lm_head_topk(*ok[:5], 0, *ok[6:]) == q4.Q4_ERR_INVALID_ARG             # top_k = 0
+    assert lib.q4_lm_head_topk(*ok[:3], 4, *ok[4:]) == q4.Q4_ERR_INVALID_ARG             # N < top_k
+    assert lib.q4_lm_head_topk(*ok[:4], 96, *ok[5:]) == q4.Q4_ERR_UNSUPPORTED_SHAPE      # K % 64
+    assert lib.q4_lm_head_topk(*ok[:6], 0.0, *ok[7:]) == q4.Q4_ERR_INVALID_ARG           # temperature
+    assert lib.q4_lm_head_topk(*ok[:8], 24, *ok[9:]) == q4.Q4_ERR_MISALIGNED             # idx
+    assert lib.q4_lm_head_topk(None, *ok[1:]) == q4.Q4_ERR_INVALID_ARG

@@ -110,3 +110,34 @@ def test_after_lm_head_matmul():
     ref_i, ref_p = T.topk_probs(y.cpu().numpy(), 32, 1.0, 0.95)
     assert np.array_equal(idx.cpu().numpy(), ref_i)
     assert np.allclose(pr.cpu().numpy(), ref_p, rtol=3e-7, atol=1e-30)
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_fused_head_equals_matmul_then_epilogue(M):
+    """q4_lm_head_topk (logits in the library's scratch, discarded from L2 after
+    the epilogue reads them) gives the same bits as q4_matmul + q4_topk_probs,
+    call after call (the scratch is rewritten each time)."""
+    N, K = si.SHAPES["lm_head"]
+    W = si.make_weights(N, K, si.w_seed(4), device="cuda")
+    for seed in (1, 2):
+        x = si.make_x(M, K, si.x_seed(4) + 10 * M + seed, device="cuda")
+        i_f, p_f = q4.lm_head_topk(x, W, N, K, 32, 0.9, 0.95)
+        y = q4.matmul(x, W, N, K)
+        i_s, p_s = q4.topk_probs(y, 32, 0.9, 0.95)
+        q4.device_status()
+        assert torch.equal(i_f, i_s) and torch.equal(p_f, p_s)
+
+
+def test_fused_head_ragged_rows():
+    """A row length that is not a multiple of 32 floats: slices that do not end
+    on a 128-byte line keep their boundary lines (only whole lines are dropped)."""
+    N, K = 40009, 1024
+    W = si.make_weights(N, K, 77, device="cuda")
+    x = si.make_x(5, K, 78, device="cuda")
+    i_f, p_f = q4.lm_head_topk(x, W, N, K, 20, 1.3, 0.8)
+    y = q4.matmul(x, W, N, K)
+    i_s, p_s = q4.topk_probs(y, 20, 1.3, 0.8)
+    q4.device_status()
+    assert torch.equal(i_f, i_s) and torch.equal(p_f, p_s)
+    ref_i, _ = T.topk_probs(y.cpu().numpy(), 20, float(np.float32(1.3)), float(np.float32(0.8)))
+    assert np.array_equal(i_f.cpu().numpy(), ref_i)
