@@ -110,20 +110,34 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of what the dominant kernel is made of: its header, the PTX wrappers
-    it uses and the host function that launches it (box, grid, split)."""
+def _strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (comment edits do not change a kernel)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
+def kernel_source_hash(texts=None):
+    """Hash of what the dominant kernel is made of, comments removed: its header,
+    the PTX wrappers it uses and the host function that launches it (box, grid,
+    split).  `texts` (name -> source) replaces the files on disk."""
     csrc = os.path.join(ROOT, "bit_row_speculative_gb300", "csrc")
+
+    def read(fn):
+        if texts is not None:
+            return texts[fn]
+        with open(os.path.join(csrc, fn)) as fh:
+            return fh.read()
+
     h = hashlib.sha256()
     for fn in ("q4_tm.cuh", "q4_sm100.cuh"):
-        with open(os.path.join(csrc, fn), "rb") as fh:
-            h.update(fn.encode())
-            h.update(fh.read())
-    with open(os.path.join(csrc, "q4_abi.cu")) as fh:
-        abi = fh.read()
+        h.update(fn.encode())
+        h.update(_strip_comments(read(fn)).encode())
+    abi = read("q4_abi.cu")
     i = abi.find("q4_status launch_tm(")
     j = abi.find("\n}\n", i)
-    h.update(abi[i:j].encode() if i >= 0 and j > i else abi.encode())
+    h.update(_strip_comments(abi[i:j] if i >= 0 and j > i else abi).encode())
     return h.hexdigest()[:16]
 
 

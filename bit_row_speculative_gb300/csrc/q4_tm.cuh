@@ -19,37 +19,41 @@
 // fold applies s * 2^33.  (|x| must stay below 2^28 for x * 2^100 to be finite.)
 //
 // Two kernels per call, chained by programmatic dependent launch:
-//   xrec_kernel  writes each group's 2112-byte x record to global scratch:
-//                the fp32 group sums X[0..15], then the M <= 16 rows of x for
-//                the group's 64 inputs as tensor-core core matrices (8 rows x
-//                8 inputs, 128 B each): rows 0-7 for the 8 input blocks, then
-//                rows 8-15.  Inputs of each 8-block are in the dequantized
-//                order k0 k4 k1 k5 k2 k6 k3 k7 and scaled as above; rows >= M
-//                are zero.  A kernel for M <= 8 copies only the first 1088
-//                bytes (X and rows 0-7).
+//   xrec_kernel  writes each group's x record to global scratch: the fp32
+//                group sums X[0..W-1], then the rows of x for the group's 64
+//                inputs as tensor-core core matrices (8 rows x 8 inputs, 128 B
+//                each), 8-row blocks one after another (2112 bytes at W = 16,
+//                4224 at W = 32; W = 16 for M <= 16, 32 for M <= 32).  Inputs
+//                of each 8-block are in the dequantized order k0 k4 k1 k5 k2
+//                k6 k3 k7 and scaled as above; rows >= M are zero.  A kernel
+//                for M <= 8 copies only the first 1088 bytes (X and rows 0-7).
+//                Inside a chained pass the glue kernel writes the records
+//                instead, and this kernel is not launched.
 //   q4_tm_kernel one persistent CTA per SM, 16 warps; tiles of 128 rows, a
 //                stage is two groups (128 inputs) of one tile.
 //     warp 0       producer: per stage one 128-row x 64-byte nibble box (TMA,
-//                  64-byte swizzle) into a ring of kStages slots, and bulk
-//                  copies of the two x records into the same slot.  The weight
-//                  boxes of the first kStages stages are issued before the
-//                  kernel waits for its predecessor (they need nothing from
-//                  it); every record copy comes after that wait.
+//                  64-byte swizzle) into a ring of slots, and bulk copies of
+//                  the two x records into the same slot.  The weight boxes of
+//                  the first ring-full of stages are issued before the kernel
+//                  waits for its predecessor (they need nothing from it);
+//                  every record copy comes after that wait.
 //     warps 1..3   MMA issuers, one per team: per stage of the team 8 MMAs
-//                  M128 N16 K16 (A = the dequantized weights in the team's
-//                  tensor memory, B = the x records in shared memory, D = the
-//                  team's P) and a commit to the team's "done" barrier.
+//                  M128 N16 K16 per 16 rows of W (A = the dequantized weights
+//                  in the team's tensor memory, B = the x records in shared
+//                  memory, D = the team's P) and a commit to the team's "done"
+//                  barrier.
 //     warps 4..15  three consumer teams of 4 warps; stage i belongs to team
 //                  i % 3.  Every team covers all 128 rows (one row per
-//                  thread) and keeps two A buffers: in its iteration for stage
-//                  i it dequantizes stage i into one buffer while the MMAs of
-//                  its previous stage (i - 3) finish on the other, then folds
-//                  that previous stage's P into its own fp32 sums with s, r
-//                  and X, frees that stage's slot and hands stage i over.  So
-//                  the tensor core and the consumers overlap within a team,
-//                  and the three teams overlap with each other.  At the end of
-//                  each tile segment the teams' sums are added in team order
-//                  through shared memory.
+//                  thread).  At W = 16 a team keeps two A buffers: in its
+//                  iteration for stage i it dequantizes stage i into one
+//                  buffer while the MMAs of its previous stage (i - 3) finish
+//                  on the other, then folds that previous stage's P into its
+//                  own fp32 sums with s, r and X, frees that stage's slot and
+//                  hands stage i over.  At W = 32 (one A buffer, to fit tensor
+//                  memory) it folds the previous stage first.  The three teams
+//                  overlap with each other.  At the end of each tile segment
+//                  the teams' sums are added in team order through shared
+//                  memory.
 // The ring has a multiple of 3 slots, so a slot always serves the same team,
 // and every barrier is waited on by threads that pass through its phases in
 // order (a parity wait never sees a phase two steps away).
