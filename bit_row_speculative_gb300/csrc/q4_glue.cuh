@@ -23,15 +23,17 @@
 // Arithmetic: the definition is evaluated as if in double, at single-precision
 // cost.  The sum of squares is kept as an unevaluated pair of floats (each
 // square split exactly by an fma, the pairs added with error-free two-sums),
-// which carries about 48 significant bits.  Each CTA reduces its slice in a
-// fixed order (thread-strided partials, then a fixed tree over lanes and
-// warps); the slices are then combined in cluster-rank order through
-// distributed shared memory, and the scale 1/sqrt(ss/K + eps) is formed in
-// double.  Each output is first computed in float; only when that value lies
-// within a few float ulps of a bf16 rounding boundary -- where float error
-// could decide the rounding -- is the element recomputed entirely in double
-// (exp included) and rounded from there.  Each row's result depends on that
-// row and K alone.
+// which carries about 48 significant bits.  Each thread takes 8-input blocks
+// (t, t + 256, ... of its slice) and adds their squares in increasing k; the
+// threads' sums go through a fixed tree over lanes and warps; the slices are
+// then combined in cluster-rank order through distributed shared memory, and
+// the scale 1/sqrt(ss/K + eps) is formed in double.  y is read once: a
+// thread's first two blocks stay in registers for the outputs (all of a
+// slice up to 4096 inputs).  Each output is first computed in float (within
+// about 4.5 float ulps of exact); only when it lies within 8 float ulps of a
+// bf16 rounding midpoint -- where float error could decide the rounding -- is
+// the element recomputed entirely in double (exp included) and rounded from
+// there.  Each row's result depends on that row and K alone.
 // Programmatic dependent launch: the kernel lets the next kernel start at once
 // and reads y only after the preceding kernel finished.  The cluster barrier is
 // a hardware barrier among CTAs that are always co-scheduled.
@@ -51,17 +53,12 @@ constexpr int kMaxSlices = 8;                 // portable cluster size
 constexpr int64_t kSliceMin = 1024;           // inputs per slice below which fewer slices are used
 // An output computed in float is trusted unless its low 16 bits (the bits
 // bf16 rounding drops) are within this many float ulps of the halfway point.
-constexpr int kTieMargin = 16;
+constexpr int kTieMargin = 8;                 // the float value is within about 4.5 ulps of exact
+constexpr int kKeep = 2;                      // 8-input blocks per thread held in registers (slices <= 4096 inputs)
 
 inline int slices(int64_t K) {
     int64_t s = (K + kSliceMin - 1) / kSliceMin;
     return (int)(s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s));
-}
-
-__device__ __forceinline__ float value_f(const float* yr, int64_t K, int64_t k, int kind) {
-    const float a = yr[k];
-    if (kind == 2) return a / (1.0f + expf(-a)) * yr[K + k];
-    return a;
 }
 
 __device__ __forceinline__ double value_d(const float* yr, int64_t K, int64_t k, int kind) {
@@ -70,12 +67,12 @@ __device__ __forceinline__ double value_d(const float* yr, int64_t K, int64_t k,
     return a;
 }
 
-// One output x[m, k] as bf16 bits: computed in float and rounded, unless it lies
-// within kTieMargin float ulps of a bf16 rounding midpoint, where it is
-// recomputed in double and rounded from there.
-__device__ __forceinline__ uint16_t output_bits(const float* yr, int64_t K, int64_t k, int kind, double inv,
+// One output x[m, k] as bf16 bits from its fp32 value v: v * inv rounded in
+// float, unless that lies within kTieMargin float ulps of a bf16 rounding
+// midpoint, where the value is recomputed in double and rounded from there.
+__device__ __forceinline__ uint16_t output_bits(float v, const float* yr, int64_t K, int64_t k, int kind, double inv,
                                                 float inv_f) {
-    const float t = __fmul_rn(value_f(yr, K, k, kind), inv_f);
+    const float t = __fmul_rn(v, inv_f);
     const int low = (int)(__float_as_uint(t) & 0xFFFFu);
     __nv_bfloat16 h;
     if (abs(low - 0x8000) <= kTieMargin)
@@ -95,6 +92,29 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float p, float e) {
 }
 
 // grid (S, M), cluster (S, 1, 1): CTA (s, m) owns inputs [s*L, min(K, (s+1)*L)) of row m.
+// The 8 values v_k, k = kb .. kb+7 (kb a multiple of 8), in fp32, loads first.
+__device__ __forceinline__ void values8(const float* yr, int64_t K, int64_t kb, int kind, bool vec, float (&v)[8]) {
+    float a[8], b[8];
+    if (vec) {
+        const float4 a0 = __ldcg(reinterpret_cast<const float4*>(yr + kb));
+        const float4 a1 = __ldcg(reinterpret_cast<const float4*>(yr + kb + 4));
+        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+        if (kind == 2) {
+            const float4 b0 = __ldcg(reinterpret_cast<const float4*>(yr + K + kb));
+            const float4 b1 = __ldcg(reinterpret_cast<const float4*>(yr + K + kb + 4));
+            b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            a[e] = __ldcg(yr + kb + e);
+            if (kind == 2) b[e] = __ldcg(yr + K + kb + e);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = kind == 2 ? a[e] / (1.0f + expf(-a[e])) * b[e] : a[e];
+}
+
 // x: bf16 [M, K] (x mode) or nullptr; rec: the next matmul's records [K/64][rec_bytes(rec_w)] (record mode) or nullptr.
 __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict__ y, int64_t n_prev, int64_t K,
                                                         int kind, double eps, uint16_t* __restrict__ x,
@@ -102,6 +122,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     namespace cg = cooperative_groups;
     __shared__ float part_hi[kThreads / 32], part_lo[kThreads / 32];
     __shared__ float slice_sum[2];
+    __shared__ double inv_s;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");     // y comes from the preceding kernel
     cg::cluster_group cluster = cg::this_cluster();
@@ -111,25 +132,37 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     const int64_t L = (K / 64 + S - 1) / S * 64;     // whole groups
     const int64_t k0 = (int64_t)s * L;
     const int64_t k1 = (k0 + L < K) ? k0 + L : K;
+    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8; // 8-input blocks of this slice; thread t takes t, t + 256, ...
     const float* yr = y + (int64_t)m * n_prev;
+    const bool vec = (n_prev & 3) == 0;              // rows 16-byte aligned
 
+    // 1. the sum of squares: each thread's blocks in increasing k; the first kKeep blocks
+    //    stay in registers for step 2 (all their loads in flight together)
+    float keep[kKeep][8];
     float hi = 0.0f, lo = 0.0f;
-    int64_t k = k0 + threadIdx.x;
-    // four independent loads in flight per thread, then the squares in increasing k
-    for (; k + 3 * kThreads < k1; k += 4 * kThreads) {
-        float v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = value_f(yr, K, k + u * kThreads, kind);
+    for (int u = 0; u < kKeep; ++u) {
+        const int64_t b = threadIdx.x + (int64_t)u * kThreads;
+        if (b < nblk) values8(yr, K, k0 + 8 * b, kind, vec, keep[u]);
+    }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float p = __fmul_rn(v[u], v[u]);
-            ff_add(hi, lo, p, __fmaf_rn(v[u], v[u], -p));
+    for (int u = 0; u < kKeep; ++u) {
+        if ((int64_t)threadIdx.x + (int64_t)u * kThreads < nblk) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float p = __fmul_rn(keep[u][e], keep[u][e]);
+                ff_add(hi, lo, p, __fmaf_rn(keep[u][e], keep[u][e], -p));
+            }
         }
     }
-    for (; k < k1; k += kThreads) {
-        const float v = value_f(yr, K, k, kind);
-        const float p = __fmul_rn(v, v);
-        ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
+    for (int64_t b = threadIdx.x + (int64_t)kKeep * kThreads; b < nblk; b += kThreads) {
+        float v[8];
+        values8(yr, K, k0 + 8 * b, kind, vec, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float p = __fmul_rn(v[e], v[e]);
+            ff_add(hi, lo, p, __fmaf_rn(v[e], v[e], -p));
+        }
     }
     // fixed tree: lanes, then warps in order
 #pragma unroll
@@ -149,7 +182,6 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         slice_sum[1] = tl;
     }
     cluster.sync();                                   // every slice's sum is in its CTA's shared memory
-    __shared__ double inv_s;
     if (threadIdx.x == 0) {
         float th = 0.0f, tl = 0.0f;
         for (int r = 0; r < S; ++r) {                 // slices in rank order
@@ -161,24 +193,31 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     cluster.sync();                                   // no CTA leaves while another still reads its sum
     const double inv = inv_s;
     const float inv_f = (float)inv;
-    if (rec == nullptr) {
-        uint16_t* xr = x + (int64_t)m * K;
-        for (int64_t kk = k0 + threadIdx.x; kk < k1; kk += kThreads) xr[kk] = output_bits(yr, K, kk, kind, inv, inv_f);
-        return;
-    }
-    // record mode: thread b takes the 8-block of inputs k0 + 8b .. k0 + 8b + 7; the
-    // 8 blocks of a group sit in 8 consecutive lanes (slices are whole groups)
-    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8;
+
+    // 2. the outputs, block by block (uniform over the CTA: whole warps take part)
     const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
-    for (int64_t b0 = 0; b0 < nblk; b0 += kThreads) {      // uniform over the CTA: whole warps take part
+    auto emit = [&](int64_t b0, const float (&v)[8]) {
         const int64_t b = b0 + threadIdx.x;
         const bool active = b < nblk;
+        const int64_t kb = k0 + 8 * b;                // first input of the block
         uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (active) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) h[e] = output_bits(yr, K, k0 + 8 * b + e, kind, inv, inv_f);
+            for (int e = 0; e < 8; ++e) h[e] = output_bits(v[e], yr, K, kb + e, kind, inv, inv_f);
         }
-        // the group sum X: the 8 values in increasing k, then the 8 blocks by a fixed xor tree
+        if (rec == nullptr) {
+            if (active) {
+                uint4 o;
+                o.x = h[0] | (h[1] << 16);
+                o.y = h[2] | (h[3] << 16);
+                o.z = h[4] | (h[5] << 16);
+                o.w = h[6] | (h[7] << 16);
+                *reinterpret_cast<uint4*>(x + (int64_t)m * K + kb) = o;
+            }
+            return;
+        }
+        // record mode: the group sum X, the 8 values in increasing k, then the 8 blocks of the
+        // group (8 consecutive lanes: slices are whole groups) by a fixed xor tree
         float sx = 0.0f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) sx = __fadd_rn(sx, __uint_as_float(h[e] << 16));
@@ -186,11 +225,10 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 2));
         sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 4));
         if (active) {
-            const int64_t kb = k0 + 8 * b;                    // first input of the block
             const int64_t g = kb / 64;
             const int kc = (int)((kb / 8) & 7);
             uint8_t* r = rec + g * rb;
-            uint4 o;                                          // pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), scaled
+            uint4 o;                                  // pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), scaled
             o.x = q4::tm::bf16x2_mul(h[0] | (h[4] << 16), q4::tm::kXScaleEven);
             o.y = q4::tm::bf16x2_mul(h[1] | (h[5] << 16), q4::tm::kXScaleOdd);
             o.z = q4::tm::bf16x2_mul(h[2] | (h[6] << 16), q4::tm::kXScaleEven);
@@ -198,6 +236,14 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
             *reinterpret_cast<uint4*>(r + rb0 + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
             if (kc == 0) reinterpret_cast<float*>(r)[m] = sx;
         }
+    };
+#pragma unroll
+    for (int u = 0; u < kKeep; ++u)
+        if ((int64_t)u * kThreads < nblk) emit((int64_t)u * kThreads, keep[u]);
+    for (int64_t b0 = (int64_t)kKeep * kThreads; b0 < nblk; b0 += kThreads) {
+        float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        if (b0 + threadIdx.x < nblk) values8(yr, K, k0 + 8 * (b0 + threadIdx.x), kind, vec, v);
+        emit(b0, v);
     }
 }
 
