@@ -70,8 +70,8 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
  *   x : device, bf16, row-major [M, K], 16-byte aligned.
  *   W : device, packed buffer of exactly q4_packed_bytes(N, K) bytes, 16-byte aligned.
  *   M : 1..32 verify rows (the pages' kernels exist for 8, 16, 24 and 32 rows:
- *       up to four lanes of eight; "Splash engine", section "The engine
- *       hard-codes the model").   N : >= 1 outputs.   K : positive multiple of 64.
+ *       up to four lanes of eight; "Splash engine", section "The decode step
+ *       is one command buffer").   N : >= 1 outputs.   K : positive multiple of 64.
  *   y : device, fp32, row-major [M, N], 16-byte aligned; fully overwritten.
  * Row invariance: row m of y is bit-identical for every M (1..32) and every
  * other row's contents.
