@@ -38,10 +38,12 @@
 //                  waits for its predecessor (they need nothing from it);
 //                  every record copy comes after that wait.
 //     warps 1..3   MMA issuers, one per team: per stage of the team 8 MMAs
-//                  M128 N16 K16 per 16 rows of W (A = the dequantized weights
-//                  in the team's tensor memory, B = the x records in shared
-//                  memory, D = the team's P) and a commit to the team's "done"
-//                  barrier.
+//                  M128 N=W K16 (A = the dequantized weights in the team's
+//                  tensor memory, B = the x records in shared memory, D = the
+//                  team's P) and a commit to the team's "done" barrier.  Each
+//                  column of an N = 32 MMA carries the same bits as the same
+//                  column of an N = 16 MMA (tested: rows at M = 17..32 equal
+//                  the rows at M <= 16), so row invariance holds across widths.
 //     warps 4..15  three consumer teams of 4 warps; stage i belongs to team
 //                  i % 3.  Every team covers all 128 rows (one row per
 //                  thread).  At W = 16 a team keeps two A buffers: in its
@@ -548,7 +550,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     } else if (warp <= kIssuers) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
         const int team = (warp - 1) / kIssuersPerTeam, gsel = (warp - 1) % kIssuersPerTeam;
-        const uint32_t idesc = idesc_bf16_f32(128, 16);
+        const uint32_t idesc = idesc_bf16_f32(128, W);
         // B: core matrices K-major, 128 B apart along K, rows 8-15 1024 B after rows 0-7
         const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(smem + kNibStage + kRecB), 128, 1024);
         const uint32_t tbase = tmem + (uint32_t)team * kColsTeam;
@@ -568,14 +570,10 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                 for (int g = 0; g < 2; ++g) {
                     if (g % kIssuersPerTeam != gsel) continue;
                     const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
-                    // P of group g: W columns, rows 0-15 then (W = 32) rows 16-31 from the
-                    // record's second 2048 bytes -- the same N = 16 instruction for every row
+                    // P of group g: W columns (N = W: the record's 8-row blocks, 1024 bytes apart)
 #pragma unroll
-                    for (int h = 0; h < W / 16; ++h)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_ts(dS + (uint32_t)W * g + 16u * h, aS + 32u * g + 8u * kk,
-                                      bg + (uint64_t)((2048 * h) >> 4) + 16u * kk, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ts(dS + (uint32_t)W * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&done[team]);
                 if (team == 0 && gsel == 0) Q4_TMTR(p, 2001 + 2 * si);
