@@ -665,7 +665,15 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         // the stage handed over in the previous iteration, folded in this one
         int pend = -1, pend_seg = 0;
         float ps0 = 0.f, pr0 = 0.f, ps1 = 0.f, pr1 = 0.f;
-        auto fold_pending = [&]() {
+        // hand the team's current stage to its issuer: its A is stored and P is free
+        auto arrive_ready = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ready[team]);
+        };
+        // signal_ready (W = 16): the hand-over happens as soon as P has been loaded into
+        // registers, so the next MMAs run while this stage's P is folded
+        auto fold_pending = [&](bool signal_ready) {
             const int pslot = pend % kStages;
             live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], (uint32_t)((pend / kTeams) & 1), 4u,
                                                                  abort_flag));
@@ -681,6 +689,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                     tmem_ld_32x32b_x8(dP, P0);
                     tmem_ld_32x32b_x8(dP + 16u, P1);
                     tmem_wait_ld();
+                    if (signal_ready) arrive_ready();
                     fold_group<MT>(acc, P0, xs0, ps0, pr0);
                     fold_group<MT>(acc, P1, xs1, ps1, pr1);
                 } else if (W == 32) {
@@ -697,9 +706,12 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                     tmem_ld_32x32b_x16(dP, P0);
                     tmem_ld_32x32b_x16(dP + 16u, P1);
                     tmem_wait_ld();
+                    if (signal_ready) arrive_ready();
                     fold_group<MT>(acc, P0, xs0, ps0, pr0);
                     fold_group<MT>(acc, P1, xs1, ps1, pr1);
                 }
+            } else if (signal_ready) {
+                arrive_ready();
             }
             // that stage's slot (nibbles, records) has been read, and so has P
             tc_fence_before();
@@ -718,7 +730,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                                                                  abort_flag));
             Q4_TMTR(p, tr + 8 * j + 1);
             // one A buffer (W = 32): the previous stage's MMAs must have read it, so fold first
-            if (a_buffers(W) == 1 && pend >= 0) fold_pending();
+            if (a_buffers(W) == 1 && pend >= 0) fold_pending(false);
             // dequantize into this stage's A buffer (at W = 16 the other one may still feed the previous MMAs)
             if (live) {
                 const uint8_t* nb = smem + slot * kStageBytes + row * 64;
@@ -741,11 +753,10 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             }
             Q4_TMTR(p, tr + 8 * j + 2);
             // fold the previous stage (its MMAs ran meanwhile); then P is free again
-            if (a_buffers(W) == 2 && pend >= 0) fold_pending();
+            const bool early = a_buffers(W) == 2 && pend >= 0;   // W = 16: hand over inside the fold
+            if (early) fold_pending(true);
             Q4_TMTR(p, tr + 8 * j + 3);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ready[team]);
+            if (!early) arrive_ready();
             Q4_TMTR(p, tr + 8 * j + 4);
             // this stage becomes the pending one; constants of the team's next stage
             pend = si;
@@ -769,7 +780,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             team_stage(si, sA, bA);
             if (si + kTeams < nst) team_stage(si + kTeams, sB, bB);
         }
-        if (pend >= 0) fold_pending();
+        if (pend >= 0) fold_pending(false);
         close_segments_before(n_seg);
     }
 
