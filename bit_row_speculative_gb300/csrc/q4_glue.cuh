@@ -33,7 +33,9 @@
 // about 4.5 float ulps of exact); only when it lies within 8 float ulps of a
 // bf16 rounding midpoint -- where float error could decide the rounding -- is
 // the element recomputed entirely in double (exp included) and rounded from
-// there.  Each row's result depends on that row and K alone.
+// there.  RMSNORM values are exact floats, so their product with the scale is
+// formed as a float pair and rounded exactly, without double arithmetic.  Each
+// row's result depends on that row and K alone.
 // Programmatic dependent launch: the kernel lets the next kernel start at once
 // and reads y only after the preceding kernel finished.  The cluster barrier is
 // a hardware barrier among CTAs that are always co-scheduled.
@@ -67,11 +69,38 @@ __device__ __forceinline__ double value_d(const float* yr, int64_t K, int64_t k,
     return a;
 }
 
-// One output x[m, k] as bf16 bits from its fp32 value v: v * inv rounded in
-// float, unless that lies within kTieMargin float ulps of a bf16 rounding
-// midpoint, where the value is recomputed in double and rounded from there.
+// bf16 bits of v * inv rounded to nearest even, where inv = ih + il (two floats
+// holding the double scale) and v is an exact float: the product is formed as
+// an unevaluated pair of floats (an exact fma split, normalised), and the pair
+// decides the rounding -- by the high part's dropped 16 bits, and at an exact
+// float midpoint by the sign of the low part.  Equal to rounding the exact
+// product, except within about 2^-48 of a bf16 midpoint.
+__device__ __forceinline__ uint16_t round_product_bf16(float v, float ih, float il) {
+    const float p = __fmul_rn(v, ih);
+    const float e = __fadd_rn(__fmaf_rn(v, ih, -p), __fmul_rn(v, il));
+    const float hi = __fadd_rn(p, e);                 // normalise: |lo| <= half an ulp of hi
+    const float lo = __fsub_rn(e, __fsub_rn(hi, p));
+    const uint32_t b = __float_as_uint(hi);
+    const uint32_t low = b & 0xFFFFu;
+    uint32_t h = b >> 16;
+    bool up;
+    if (low != 0x8000u) {
+        up = low > 0x8000u;                           // |lo| cannot move the value across the midpoint
+    } else if (lo != 0.0f) {
+        up = (lo > 0.0f) == (hi > 0.0f);              // beyond the midpoint in magnitude
+    } else {
+        up = (h & 1u) != 0u;                          // an exact tie: to even
+    }
+    return (uint16_t)(h + (up ? 1u : 0u));
+}
+
+// One output x[m, k] as bf16 bits from its fp32 value v.  RMSNORM (v exact):
+// round_product_bf16.  SWIGLU (v within about 4.5 float ulps of exact): v * inv
+// rounded in float, unless that lies within kTieMargin float ulps of a bf16
+// rounding midpoint, where the value is recomputed in double.
 __device__ __forceinline__ uint16_t output_bits(float v, const float* yr, int64_t K, int64_t k, int kind, double inv,
-                                                float inv_f) {
+                                                float inv_f, float inv_lo) {
+    if (kind != 2) return round_product_bf16(v, inv_f, inv_lo);
     const float t = __fmul_rn(v, inv_f);
     const int low = (int)(__float_as_uint(t) & 0xFFFFu);
     __nv_bfloat16 h;
@@ -193,6 +222,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     cluster.sync();                                   // no CTA leaves while another still reads its sum
     const double inv = inv_s;
     const float inv_f = (float)inv;
+    const float inv_lo = (float)(inv - (double)inv_f);
 
     // 2. the outputs, block by block (uniform over the CTA: whole warps take part)
     const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
@@ -203,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (active) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) h[e] = output_bits(v[e], yr, K, kb + e, kind, inv, inv_f);
+            for (int e = 0; e < 8; ++e) h[e] = output_bits(v[e], yr, K, kb + e, kind, inv, inv_f, inv_lo);
         }
         if (rec == nullptr) {
             if (active) {

@@ -19,7 +19,6 @@ from parity import check_tolerance, sample_columns, xbits
 
 pytestmark = pytest.mark.gpu
 
-GLUE_ULP_RATE = 1e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,16 +48,39 @@ def _check_layer(x: torch.Tensor, W: torch.Tensor, N: int, K: int, y: torch.Tens
     check_tolerance(y.cpu().numpy()[:, cols], ref, scale, what)
 
 
+def _bf16_value(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def _check_glue(y: torch.Tensor, K_next: int, kind: int, x_next: torch.Tensor, what: str):
-    """GPU glue output against the oracle's glue of the same fp32 y."""
+    """GPU glue output against the oracle's glue of the same fp32 y.  A differing
+    element must be one bf16 ulp away and lie at a tie: its value (recomputed here
+    in double only to classify the difference) is within `rel` of the midpoint
+    between the two candidates.  RMSNORM: rel = 1e-9 (the kernel's scale agrees
+    with an all-double one to about 1e-14).  SWIGLU: rel = 2e-6, because the
+    kernel's sum of squares is taken over the fp32 values silu(a) * b, each within
+    about 9 float ulps of exact, so its scale is within about 5e-7 of the
+    all-double one."""
     ref = oracle.glue(y.cpu().numpy(), K_next, kind)
     got = si.bf16_bits(x_next.cpu()).numpy().view(np.uint16)
     diff = got != ref
-    if diff.any():
-        # 1 ulp in bf16 (same sign) and rare
-        d = np.abs(got[diff].astype(np.int32) - ref[diff].astype(np.int32))
-        assert int(d.max()) <= 1, f"{what}: glue differs from the oracle by {int(d.max())} ulp"
-        assert diff.mean() <= GLUE_ULP_RATE, f"{what}: glue 1-ulp differences at rate {diff.mean():.2e}"
+    if not diff.any():
+        return
+    d = np.abs(got[diff].astype(np.int32) - ref[diff].astype(np.int32))
+    assert int(d.max()) <= 1, f"{what}: glue differs from the oracle by {int(d.max())} ulp"
+    yy = y.cpu().numpy().astype(np.float64)
+    if kind == q4.GLUE_SWIGLU_RMSNORM:
+        a = yy[:, :K_next]
+        v = a / (1.0 + np.exp(-a)) * yy[:, K_next:2 * K_next]
+    else:
+        v = yy[:, :K_next]
+    inv = 1.0 / np.sqrt(np.mean(v * v, axis=1, keepdims=True) + 1e-6)
+    t = (v * inv)[diff]
+    mid = 0.5 * (_bf16_value(got[diff]) + _bf16_value(ref[diff]))
+    rel = np.abs(t - mid) / np.maximum(np.abs(t), 1e-300)
+    lim = 2e-6 if kind == q4.GLUE_SWIGLU_RMSNORM else 1e-9
+    assert np.all(rel <= lim), (f"{what}: {int(np.sum(rel > lim))} of {int(diff.sum())} differing outputs are not "
+                                f"at a bf16 tie (max distance {rel.max():.3g})")
 
 
 def _run_by_layers(layers, x0, checks=True, sample=None, tag=""):
