@@ -115,14 +115,18 @@ q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int6
  * x_{j+1} of the next.  The pages' own between-layer operators (attention,
  * Gated DeltaNet, gated norms) are outside the matmul path; this library joins
  * layers with a fixed, bounded stand-in ("Splash engine" analysis, section
- * "Everything in one command buffer": one submission runs every layer of the
- * step in order):
+ * "The decode step is one command buffer": one submission runs every layer of
+ * the step in order):
  *   RMSNORM:        v_k = y[m, k] for the first K_next columns (K_next <= N_prev)
  *   SWIGLU_RMSNORM: v_k = silu(y[m, k]) * y[m, K_next + k]       (N_prev == 2 K_next)
  *   x[m, k] = bf16_RNE( v_k / sqrt( mean_k v_k^2 + 1e-6 ) ),  silu(a) = a / (1 + e^-a)
- * The sum of squares and the scaling are done in double, so the one rounding
- * to bf16 matches an all-double evaluation except, rarely, where expf's
- * single-precision rounding decides a tie-near value. */
+ * Accuracy: the sum of squares is carried in about 48 bits and the scale formed
+ * in double.  RMSNORM: the one rounding to bf16 matches an all-double
+ * evaluation except where the value lies within about 1e-14 of a bf16 midpoint.
+ * SWIGLU: silu(a) * b is formed in fp32 (within about 9 float ulps), with a
+ * double recomputation near a bf16 midpoint; the scale agrees with an
+ * all-double one to about 1e-8, so an output may differ by one bf16 ulp where
+ * its value lies within about 5e-7 of a midpoint. */
 typedef enum {
     Q4_GLUE_NONE = 0,              /* last layer: its y is the step's output  */
     Q4_GLUE_RMSNORM = 1,
