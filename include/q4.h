@@ -156,7 +156,7 @@ q4_status q4_glue(const float* y, int M, int64_t N_prev, int64_t K_next, int glu
 size_t q4_decode_step_workspace_bytes(const q4_layer* layers, int n_layers, int M);
 
 /* One decode step of the chained verify pass in one submission ("Splash
- * engine", section "Everything in one command buffer"): for j = 0..n-1,
+ * engine", section "The decode step is one command buffer"): for j = 0..n-1,
  * y_j = x_j * W_j^T (as q4_matmul) and x_{j+1} = glue_j(y_j); the last layer
  * writes y_last [M, N_{n-1}] (fp32, device, 16-byte aligned).  x0 is bf16
  * [M, K_0] on the device.  Every kernel is chained with programmatic dependent

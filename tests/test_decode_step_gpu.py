@@ -1,5 +1,5 @@
 """q4_decode_step and q4_glue on the GPU: the chained verify pass ("Splash
-engine" analysis, section "Everything in one command buffer": every layer of
+engine" analysis, section "The decode step is one command buffer": every layer of
 the step runs in order in one submission).
 
 Teacher-forced checks: each layer's GPU output is compared with the oracle
