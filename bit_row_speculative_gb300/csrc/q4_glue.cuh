@@ -20,22 +20,30 @@
 // into the record layout, and the group sums X added in the record kernel's
 // order -- so that matmul needs no record kernel and x_next is never stored.
 //
-// Arithmetic: the definition is evaluated as if in double, at single-precision
-// cost.  The sum of squares is kept as an unevaluated pair of floats (each
-// square split exactly by an fma, the pairs added with error-free two-sums),
-// which carries about 48 significant bits.  Each thread takes 8-input blocks
-// (t, t + 256, ... of its slice) and adds their squares in increasing k; the
-// threads' sums go through a fixed tree over lanes and warps; the slices are
-// then combined in cluster-rank order through distributed shared memory, and
-// the scale 1/sqrt(ss/K + eps) is formed in double.  y is read once: a
-// thread's first two blocks stay in registers for the outputs (all of a
-// slice up to 4096 inputs).  Each output is first computed in float (within
-// about 4.5 float ulps of exact); only when it lies within 8 float ulps of a
-// bf16 rounding midpoint -- where float error could decide the rounding -- is
-// the element recomputed entirely in double (exp included) and rounded from
-// there.  RMSNORM values are exact floats, so their product with the scale is
-// formed as a float pair and rounded exactly, without double arithmetic.  Each
-// row's result depends on that row and K alone.
+// Arithmetic: the definition is evaluated as if in double, on the
+// single-precision pipes.  The sum of squares is kept as an unevaluated pair of
+// floats (each square split exactly by an fma, the pairs added with error-free
+// two-sums), which carries about 48 significant bits.  Each thread takes 8-input
+// blocks (t, t + 256, ... of its slice) and adds their squares in increasing k;
+// the threads' sums go through a fixed tree over lanes and warps; the slices
+// are combined in cluster-rank order through distributed shared memory, and the
+// scale 1/sqrt(ss/K + eps) is formed in double and split into two floats.  y is
+// read once: a thread's first two blocks stay in registers for the outputs (all
+// of a slice up to 4096 inputs).
+//   RMSNORM: v is an exact float, so v * scale is formed as a normalised float
+//   pair and rounded to bf16 from it (the dropped 16 bits of the high part, and
+//   at an exact float midpoint the sign of the low part): the rounding of the
+//   exact product, except within about 2^-48 of a bf16 midpoint.
+//   SWIGLU: silu(a) * b is formed in fp32 (within 9 float ulps); the output is
+//   rounded from its fp32 product with the scale unless that lies within 10
+//   float ulps of a bf16 midpoint, where v is recomputed in float pairs from the
+//   inputs kept in registers (e^-a by
+//   range reduction with ln 2 split into three floats and a Taylor series, then
+//   a pair division; about 1e-14) and rounded from the pair.  Its sum of squares
+//   is over the fp32 values, so its scale is within about 5e-7 of an all-double
+//   one (typically 1e-8).
+// No double arithmetic per element.  Each row's result depends on that row and
+// K alone.
 // Programmatic dependent launch: the kernel lets the next kernel start at once
 // and reads y only after the preceding kernel finished.  The cluster barrier is
 // a hardware barrier among CTAs that are always co-scheduled.
@@ -55,7 +63,7 @@ constexpr int kMaxSlices = 8;                 // portable cluster size
 constexpr int64_t kSliceMin = 1024;           // inputs per slice below which fewer slices are used
 // An output computed in float is trusted unless its low 16 bits (the bits
 // bf16 rounding drops) are within this many float ulps of the halfway point.
-constexpr int kTieMargin = 8;                 // the float value is within about 4.5 ulps of exact
+constexpr int kTieMarginSwiglu = 10;          // SWIGLU: the fp32 output is within 9 float ulps of exact
 constexpr int kKeep = 2;                      // 8-input blocks per thread held in registers (slices <= 4096 inputs)
 
 inline int slices(int64_t K) {
@@ -63,26 +71,92 @@ inline int slices(int64_t K) {
     return (int)(s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s));
 }
 
-__device__ __forceinline__ double value_d(const float* yr, int64_t K, int64_t k, int kind) {
-    const double a = (double)yr[k];
-    if (kind == 2) return a / (1.0 + exp(-a)) * (double)yr[K + k];
-    return a;
+// ---- float pairs (an unevaluated hi + lo, about 48 significant bits) ----
+struct fpair {
+    float hi, lo;
+};
+
+__device__ __forceinline__ fpair fast_two_sum(float a, float b) {   // |a| >= |b|
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
 }
 
-// bf16 bits of v * inv rounded to nearest even, where inv = ih + il (two floats
-// holding the double scale) and v is an exact float: the product is formed as
-// an unevaluated pair of floats (an exact fma split, normalised), and the pair
-// decides the rounding -- by the high part's dropped 16 bits, and at an exact
-// float midpoint by the sign of the low part.  Equal to rounding the exact
-// product, except within about 2^-48 of a bf16 midpoint.
-__device__ __forceinline__ uint16_t round_product_bf16(float v, float ih, float il) {
-    const float p = __fmul_rn(v, ih);
-    const float e = __fadd_rn(__fmaf_rn(v, ih, -p), __fmul_rn(v, il));
-    const float hi = __fadd_rn(p, e);                 // normalise: |lo| <= half an ulp of hi
-    const float lo = __fsub_rn(e, __fsub_rn(hi, p));
+__device__ __forceinline__ fpair two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ fpair pair_add(fpair a, fpair b) {
+    fpair s = two_sum(a.hi, b.hi);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ fpair pair_mul(fpair a, fpair b) {
+    const float p = __fmul_rn(a.hi, b.hi);
+    const float e = __fadd_rn(__fmaf_rn(a.hi, b.hi, -p), __fadd_rn(__fmul_rn(a.hi, b.lo), __fmul_rn(a.lo, b.hi)));
+    return fast_two_sum(p, e);
+}
+
+__device__ __forceinline__ fpair pair_mul_f(fpair a, float b) {
+    const float p = __fmul_rn(a.hi, b);
+    return fast_two_sum(p, __fadd_rn(__fmaf_rn(a.hi, b, -p), __fmul_rn(a.lo, b)));
+}
+
+__device__ __forceinline__ fpair f_div_pair(float a, fpair d) {   // a / d
+    const float q1 = __fdiv_rn(a, d.hi);
+    const float r = __fsub_rn(__fmaf_rn(-q1, d.hi, a), __fmul_rn(q1, d.lo));
+    return fast_two_sum(q1, __fdiv_rn(r, d.hi));
+}
+
+// exp(x) as a float pair, relative error about 1e-14 for -60 <= x <= 88 (below
+// -60 the low part turns subnormal; exp(x) < 1e-26 there).  x = k ln2 + r with
+// ln 2 split into three floats (k * L1 exact), exp(r) by its Taylor series:
+// the terms of order 7 and up in float, the rest in pairs.
+__device__ __forceinline__ fpair exp_pair(float x) {
+    const float kL1 = 0.693145751953125f;           // 16 significant bits
+    const float kL2 = __uint_as_float(0x35bfbe8eu);  // ln 2 - L1, rounded
+    const float kL3 = __uint_as_float(0x29778000u);  // ln 2 - L1 - L2, rounded
+    const float k = rintf(__fmul_rn(x, 1.44269504f));
+    const float t = __fsub_rn(x, __fmul_rn(k, kL1));  // exact
+    const float p = __fmul_rn(k, kL2);
+    const float pe = __fmaf_rn(k, kL2, -p);
+    fpair r = two_sum(t, -p);
+    r = fast_two_sum(r.hi, __fsub_rn(__fsub_rn(r.lo, pe), __fmul_rn(k, kL3)));
+    // 1/n!: n = 7..13 as floats, n = 0..6 as pairs
+    const float c_hi[7] = {__uint_as_float(0x2f309231u), __uint_as_float(0x310f76c7u), __uint_as_float(0x32d7322bu),
+                            __uint_as_float(0x3493f27eu), __uint_as_float(0x3638ef1du), __uint_as_float(0x37d00d01u),
+                            __uint_as_float(0x39500d01u)};
+    float sf = c_hi[0];
+#pragma unroll
+    for (int n = 1; n < 7; ++n) sf = __fmaf_rn(sf, r.hi, c_hi[n]);   // orders 13 .. 7
+    const uint32_t ph[7] = {0x3ab60b61u, 0x3c088889u, 0x3d2aaaabu, 0x3e2aaaabu, 0x3f000000u, 0x3f800000u, 0x3f800000u};
+    const uint32_t pl[7] = {0xae13e93fu, 0xafeeeeefu, 0xb0aaaaabu, 0xb1aaaaabu, 0u, 0u, 0u};
+    fpair S = {sf, 0.0f};
+#pragma unroll
+    for (int n = 0; n < 7; ++n)                                       // orders 6 .. 0
+        S = pair_add(pair_mul(S, r), fpair{__uint_as_float(ph[n]), __uint_as_float(pl[n])});
+    const float sc = __int_as_float(((int)k + 127) << 23);           // 2^k (-87 <= k <= 127 here)
+    return {__fmul_rn(S.hi, sc), __fmul_rn(S.lo, sc)};
+}
+
+// v_k as a float pair: y itself (RMSNORM, exact) or silu(a) * b = a * b / (1 + e^-a)
+// (SWIGLU, relative error about 1e-14).  a > 60: e^-a does not change 1 + e^-a in
+// 48 bits; a < -88: e^-a overflows a float and the value (below 1e-36 * |b|) is 0.
+__device__ __forceinline__ fpair value_pair(float a, float b, int kind) {
+    if (kind != 2) return {a, 0.0f};
+    if (a < -88.0f) return {0.0f, 0.0f};
+    const fpair d = a > 60.0f ? fpair{1.0f, 0.0f} : pair_add(exp_pair(-a), fpair{1.0f, 0.0f});
+    return pair_mul_f(f_div_pair(a, d), b);
+}
+
+// bf16 bits of the pair hi + lo (|lo| <= half an ulp of hi) rounded to nearest
+// even: by the high part's dropped 16 bits, and at an exact float midpoint by
+// the sign of the low part.
+__device__ __forceinline__ uint16_t round_pair_bf16(float hi, float lo) {
     const uint32_t b = __float_as_uint(hi);
     const uint32_t low = b & 0xFFFFu;
-    uint32_t h = b >> 16;
+    const uint32_t h = b >> 16;
     bool up;
     if (low != 0x8000u) {
         up = low > 0x8000u;                           // |lo| cannot move the value across the midpoint
@@ -94,20 +168,25 @@ __device__ __forceinline__ uint16_t round_product_bf16(float v, float ih, float 
     return (uint16_t)(h + (up ? 1u : 0u));
 }
 
-// One output x[m, k] as bf16 bits from its fp32 value v.  RMSNORM (v exact):
-// round_product_bf16.  SWIGLU (v within about 4.5 float ulps of exact): v * inv
-// rounded in float, unless that lies within kTieMargin float ulps of a bf16
-// rounding midpoint, where the value is recomputed in double.
-__device__ __forceinline__ uint16_t output_bits(float v, const float* yr, int64_t K, int64_t k, int kind, double inv,
-                                                float inv_f, float inv_lo) {
-    if (kind != 2) return round_product_bf16(v, inv_f, inv_lo);
+
+// One output x[m, k] as bf16 bits.  RMSNORM (v exact): v * scale as a
+// normalised float pair, rounded from the pair.  SWIGLU: v * scale rounded in
+// float, unless that lies within kTieMarginSwiglu float ulps of a bf16 rounding
+// midpoint (the fp32 value is within 9 ulps of exact), where it is recomputed
+// as a float pair from the inputs a and b and rounded from the pair.
+__device__ __forceinline__ uint16_t output_bits(float v, float a, float b, int kind, float inv_f, float inv_lo) {
+    if (kind != 2) {                                              // RMSNORM: the exact pair, no branch
+        const float p = __fmul_rn(v, inv_f);
+        const fpair w = fast_two_sum(p, __fadd_rn(__fmaf_rn(v, inv_f, -p), __fmul_rn(v, inv_lo)));
+        return round_pair_bf16(w.hi, w.lo);
+    }
     const float t = __fmul_rn(v, inv_f);
     const int low = (int)(__float_as_uint(t) & 0xFFFFu);
-    __nv_bfloat16 h;
-    if (abs(low - 0x8000) <= kTieMargin)
-        h = __double2bfloat16(value_d(yr, K, k, kind) * inv);   // near a tie: decide in double
-    else
-        h = __float2bfloat16_rn(t);
+    if (abs(low - 0x8000) <= (kind == 2 ? kTieMarginSwiglu : kTieMarginNorm)) {
+        const fpair w = pair_mul(value_pair(a, b, kind), fpair{inv_f, inv_lo});
+        return round_pair_bf16(w.hi, w.lo);
+    }
+    const __nv_bfloat16 h = __float2bfloat16_rn(t);
     return *reinterpret_cast<const uint16_t*>(&h);
 }
 
@@ -121,9 +200,10 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float p, float e) {
 }
 
 // grid (S, M), cluster (S, 1, 1): CTA (s, m) owns inputs [s*L, min(K, (s+1)*L)) of row m.
-// The 8 values v_k, k = kb .. kb+7 (kb a multiple of 8), in fp32, loads first.
-__device__ __forceinline__ void values8(const float* yr, int64_t K, int64_t kb, int kind, bool vec, float (&v)[8]) {
-    float a[8], b[8];
+// The inputs of the 8 values v_k, k = kb .. kb+7 (kb a multiple of 8): a = y[k]
+// and, for SWIGLU, b = y[K + k]; all loads issued together.
+__device__ __forceinline__ void inputs8(const float* yr, int64_t K, int64_t kb, int kind, bool vec, float (&a)[8],
+                                        float (&b)[8]) {
     if (vec) {
         const float4 a0 = __ldcg(reinterpret_cast<const float4*>(yr + kb));
         const float4 a1 = __ldcg(reinterpret_cast<const float4*>(yr + kb + 4));
@@ -140,8 +220,15 @@ __device__ __forceinline__ void values8(const float* yr, int64_t K, int64_t kb, 
             if (kind == 2) b[e] = __ldcg(yr + K + kb + e);
         }
     }
+    if (kind != 2) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = kind == 2 ? a[e] / (1.0f + expf(-a[e])) * b[e] : a[e];
+        for (int e = 0; e < 8; ++e) b[e] = 0.0f;
+    }
+}
+
+// v_k in fp32 (exact for RMSNORM).
+__device__ __forceinline__ float value_f(float a, float b, int kind) {
+    return kind == 2 ? a / (1.0f + expf(-a)) * b : a;
 }
 
 // x: bf16 [M, K] (x mode) or nullptr; rec: the next matmul's records [K/64][rec_bytes(rec_w)] (record mode) or nullptr.
@@ -167,30 +254,32 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
 
     // 1. the sum of squares: each thread's blocks in increasing k; the first kKeep blocks
     //    stay in registers for step 2 (all their loads in flight together)
-    float keep[kKeep][8];
+    float keep_a[kKeep][8], keep_b[kKeep][8];
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
     for (int u = 0; u < kKeep; ++u) {
         const int64_t b = threadIdx.x + (int64_t)u * kThreads;
-        if (b < nblk) values8(yr, K, k0 + 8 * b, kind, vec, keep[u]);
+        if (b < nblk) inputs8(yr, K, k0 + 8 * b, kind, vec, keep_a[u], keep_b[u]);
     }
 #pragma unroll
     for (int u = 0; u < kKeep; ++u) {
         if ((int64_t)threadIdx.x + (int64_t)u * kThreads < nblk) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float p = __fmul_rn(keep[u][e], keep[u][e]);
-                ff_add(hi, lo, p, __fmaf_rn(keep[u][e], keep[u][e], -p));
+                const float v = value_f(keep_a[u][e], keep_b[u][e], kind);
+                const float p = __fmul_rn(v, v);
+                ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
             }
         }
     }
     for (int64_t b = threadIdx.x + (int64_t)kKeep * kThreads; b < nblk; b += kThreads) {
-        float v[8];
-        values8(yr, K, k0 + 8 * b, kind, vec, v);
+        float a[8], bb[8];
+        inputs8(yr, K, k0 + 8 * b, kind, vec, a, bb);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float p = __fmul_rn(v[e], v[e]);
-            ff_add(hi, lo, p, __fmaf_rn(v[e], v[e], -p));
+            const float v = value_f(a[e], bb[e], kind);
+            const float p = __fmul_rn(v, v);
+            ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
         }
     }
     // fixed tree: lanes, then warps in order
@@ -226,14 +315,15 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
 
     // 2. the outputs, block by block (uniform over the CTA: whole warps take part)
     const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
-    auto emit = [&](int64_t b0, const float (&v)[8]) {
+    auto emit = [&](int64_t b0, const float (&a)[8], const float (&bv)[8]) {
         const int64_t b = b0 + threadIdx.x;
         const bool active = b < nblk;
         const int64_t kb = k0 + 8 * b;                // first input of the block
         uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (active) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) h[e] = output_bits(v[e], yr, K, kb + e, kind, inv, inv_f, inv_lo);
+            for (int e = 0; e < 8; ++e)
+                h[e] = output_bits(value_f(a[e], bv[e], kind), a[e], bv[e], kind, inv_f, inv_lo);
         }
         if (rec == nullptr) {
             if (active) {
@@ -269,11 +359,12 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     };
 #pragma unroll
     for (int u = 0; u < kKeep; ++u)
-        if ((int64_t)u * kThreads < nblk) emit((int64_t)u * kThreads, keep[u]);
+        if ((int64_t)u * kThreads < nblk) emit((int64_t)u * kThreads, keep_a[u], keep_b[u]);
     for (int64_t b0 = (int64_t)kKeep * kThreads; b0 < nblk; b0 += kThreads) {
-        float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        if (b0 + threadIdx.x < nblk) values8(yr, K, k0 + 8 * (b0 + threadIdx.x), kind, vec, v);
-        emit(b0, v);
+        float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        float bv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        if (b0 + threadIdx.x < nblk) inputs8(yr, K, k0 + 8 * (b0 + threadIdx.x), kind, vec, a, bv);
+        emit(b0, a, bv);
     }
 }
 

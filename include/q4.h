@@ -123,10 +123,10 @@ q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int6
  * Accuracy: the sum of squares is carried in about 48 bits and the scale formed
  * in double.  RMSNORM: the one rounding to bf16 matches an all-double
  * evaluation except where the value lies within about 1e-14 of a bf16 midpoint.
- * SWIGLU: silu(a) * b is formed in fp32 (within about 9 float ulps), with a
- * double recomputation near a bf16 midpoint; the scale agrees with an
- * all-double one to about 1e-8, so an output may differ by one bf16 ulp where
- * its value lies within about 5e-7 of a midpoint. */
+ * SWIGLU: silu(a) * b is formed in fp32 (within 9 float ulps), and recomputed in
+ * float pairs (about 1e-14) near a bf16 midpoint; the scale agrees with an
+ * all-double one to about 1e-8 (at worst 5e-7), so an output may differ by one
+ * bf16 ulp where its value lies within that distance of a midpoint. */
 typedef enum {
     Q4_GLUE_NONE = 0,              /* last layer: its y is the step's output  */
     Q4_GLUE_RMSNORM = 1,

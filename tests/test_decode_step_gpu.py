@@ -56,11 +56,10 @@ def _check_glue(y: torch.Tensor, K_next: int, kind: int, x_next: torch.Tensor, w
     """GPU glue output against the oracle's glue of the same fp32 y.  A differing
     element must be one bf16 ulp away and lie at a tie: its value (recomputed here
     in double only to classify the difference) is within `rel` of the midpoint
-    between the two candidates.  RMSNORM: rel = 1e-9 (the kernel's scale agrees
-    with an all-double one to about 1e-14).  SWIGLU: rel = 2e-6, because the
-    kernel's sum of squares is taken over the fp32 values silu(a) * b, each within
-    about 9 float ulps of exact, so its scale is within about 5e-7 of the
-    all-double one."""
+    between the two candidates.  RMSNORM: rel = 1e-9 (the kernel's scale and each
+    output are formed to about 1e-14).  SWIGLU: rel = 2e-6, because the kernel's
+    sum of squares is taken over the fp32 values silu(a) * b, each within 9 float
+    ulps of exact, so its scale is within about 5e-7 of the all-double one."""
     ref = oracle.glue(y.cpu().numpy(), K_next, kind)
     got = si.bf16_bits(x_next.cpu()).numpy().view(np.uint16)
     diff = got != ref
