@@ -182,7 +182,7 @@ __device__ __forceinline__ uint16_t output_bits(float v, float a, float b, int k
     }
     const float t = __fmul_rn(v, inv_f);
     const int low = (int)(__float_as_uint(t) & 0xFFFFu);
-    if (abs(low - 0x8000) <= (kind == 2 ? kTieMarginSwiglu : kTieMarginNorm)) {
+    if (abs(low - 0x8000) <= kTieMarginSwiglu) {
         const fpair w = pair_mul(value_pair(a, b, kind), fpair{inv_f, inv_lo});
         return round_pair_bf16(w.hi, w.lo);
     }
