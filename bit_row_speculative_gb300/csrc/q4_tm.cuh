@@ -776,9 +776,22 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             load_next(sw, bw);
             Q4_TMTR(p, tr + 8 * j + 6);
         };
-        for (int si = team; si < nst; si += 2 * kTeams) {
-            team_stage(si, sA, bA);
-            if (si + kTeams < nst) team_stage(si + kTeams, sB, bB);
+        if (W == 32) {
+            // one stage per iteration (fewer live registers at 32 rows); the prefetched
+            // pairs rotate so that each stage again finds its words in sA, bA
+            for (int si = team; si < nst; si += kTeams) {
+                team_stage(si, sA, bA);
+                const uint32_t ts = sA, tb = bA;
+                sA = sB;
+                bA = bB;
+                sB = ts;
+                bB = tb;
+            }
+        } else {
+            for (int si = team; si < nst; si += 2 * kTeams) {
+                team_stage(si, sA, bA);
+                if (si + kTeams < nst) team_stage(si + kTeams, sB, bB);
+            }
         }
         if (pend >= 0) fold_pending(false);
         close_segments_before(n_seg);
