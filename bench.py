@@ -268,7 +268,7 @@ def run_reference(args, rank, world):
             "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": value,
                              "unit": "GB/s"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(check_roofline(line)), flush=True)
 
 
 def run_reference_edges(args, world):
@@ -296,7 +296,20 @@ def run_reference_edges(args, world):
             "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": value,
                              "unit": "GB/s"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(check_roofline(line)), flush=True)
+
+
+def check_roofline(line):
+    """A measured rate above the peak is a counting error or L2 reuse, not a result:
+    flag it in the line and on stderr (a fraction up to 1.05 is allowed, the peak being
+    a measured copy, not a bound)."""
+    rf = line.get("roofline") or {}
+    frac = rf.get("frac")
+    if isinstance(frac, (int, float)) and frac > 1.05:
+        msg = f"roofline fraction {frac:.3f} above the measured peak: a counting or L2-reuse error"
+        line["warning"] = msg
+        print("WARNING: " + msg, file=sys.stderr, flush=True)
+    return line
 
 
 def e2e_pipelined(args, spec, pools, xs, ys, stream, dev, world, step_bytes, chunk=10):
@@ -568,7 +581,7 @@ def run_ours(args, rank, world, local_rank):
             line["cpu_baseline"] = cpu_oracle_sample(spec, args.cpu_seconds)
         except Exception as exc:                     # report, do not hide
             line["cpu_baseline"] = {"error": repr(exc)}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(check_roofline(line)), flush=True)
 
 
 def run_full_pass(args, rank, world, local_rank):
@@ -703,7 +716,7 @@ def run_full_pass(args, rank, world, local_rank):
             line["cpu_baseline"] = cpu_oracle_sample(workload_spec("full_pass")[0], args.cpu_seconds)
         except Exception as exc:                     # report, do not hide
             line["cpu_baseline"] = {"error": repr(exc)}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(check_roofline(line)), flush=True)
 
 
 EDGE_METRIC = "draft_select_edges: algorithmic GB/s of the gathered codebook rows, hidden, ids and scores"
@@ -889,7 +902,7 @@ def run_edges(args, rank, world, local_rank):
             line["cpu_baseline"] = cpu_edges_sample(pb, sb, host_inputs, min(args.cpu_seconds, 10.0))
         except Exception as exc:                     # report, do not hide
             line["cpu_baseline"] = {"error": repr(exc)}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(check_roofline(line)), flush=True)
 
 
 def main():

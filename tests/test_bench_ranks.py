@@ -72,3 +72,11 @@ def test_reference_arm_under_torchrun_world2():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_roofline_above_peak_is_flagged():
+    import bench
+    flagged = bench.check_roofline({"roofline": {"frac": 1.3}})
+    assert "warning" in flagged
+    assert "warning" not in bench.check_roofline({"roofline": {"frac": 0.29}})
+    assert "warning" not in bench.check_roofline({"impl": "reference"})
