@@ -26,7 +26,8 @@
 //  4. The last CTA of the row to finish (an acq_rel ticket) merges the S sorted
 //     lists (the top 32 of the union of two sorted lists is the elementwise
 //     maximum of one list and the other reversed, merged bitonically), and one
-//     warp forms the probabilities in double:
+//     warp forms the probabilities in float pairs (about 48 bits, rounding like
+//     double ones; an exponential below e^-60 in double):
 //     p_j = exp((l_j - l_0)/T) / sum_i exp((l_i - l_0)/T) over the top_k, the
 //     shortest prefix whose cumulative probability reaches top_p kept (all if
 //     top_p >= 1), renormalized; fp32 probabilities and int32 indices out
@@ -36,6 +37,8 @@
 #pragma once
 
 #include <cstdint>
+
+#include "q4_pair.cuh"
 
 namespace q4 {
 namespace topk {
@@ -235,30 +238,50 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restri
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) a = warp_merge_desc(umax(a, lists[w][31 - lane]), lane);
 
-    // lane j holds the rank-j candidate.  Probabilities in double: exponentials
-    // lane-parallel, the sum as a butterfly and the cumulative sums as a scan (a
-    // fixed order; it differs from a left-to-right sum by double roundings only)
-    const double l0 = (double)key_value((uint32_t)(__shfl_sync(kFull, a, 0) >> 32));
-    const double lj = (double)key_value((uint32_t)(a >> 32));
-    const double e = lane < top_k ? exp((lj - l0) / (double)temperature) : 0.0;
-    double total = e;
+    // lane j holds the rank-j candidate.  Probabilities in float pairs (about
+    // 48 significant bits, so they round like double-precision ones):
+    // exponentials lane-parallel, the sum as a butterfly and the cumulative sums
+    // as a scan (a fixed order; it differs from a left-to-right sum by roundings
+    // of about 1e-14 only)
+    using namespace q4::pair;
+    const float f0 = key_value((uint32_t)(__shfl_sync(kFull, a, 0) >> 32));
+    const float fj = key_value((uint32_t)(a >> 32));
+    fpair e = {0.0f, 0.0f};
+    if (lane < top_k) {
+        const fpair x = pair_div_f(two_sum(fj, -f0), temperature);   // (l_j - l_0) / T, <= 0
+        if (x.hi >= -60.0f) {
+            // exp(x.hi + x.lo) = exp(x.hi) * (1 + x.lo + x.lo^2 / 2), |x.lo| < 4e-6
+            const float c = __fmaf_rn(__fmul_rn(0.5f, x.lo), x.lo, x.lo);
+            e = pair_mul(exp_pair(x.hi), fast_two_sum(1.0f, c));
+        } else {
+            // below e^-60 (rare: a logit gap of 60 temperatures): the exponential in double
+            const double ed = exp((double)x.hi + (double)x.lo);
+            e = fpair{(float)ed, (float)(ed - (double)(float)ed)};
+        }
+    }
+    fpair total = e;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
-    const double pj = e / total;
-    double cum = pj;                                           // inclusive scan over ranks
+    for (int o = 16; o > 0; o >>= 1) {
+        const fpair t = {__shfl_xor_sync(kFull, total.hi, o), __shfl_xor_sync(kFull, total.lo, o)};
+        total = pair_add(total, t);
+    }
+    const fpair pj = pair_div(e, total);
+    fpair cum = pj;                                            // inclusive scan over ranks
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(kFull, cum, o);
-        if (lane >= o) cum += t;
+        const fpair t = {__shfl_up_sync(kFull, cum.hi, o), __shfl_up_sync(kFull, cum.lo, o)};
+        if (lane >= o) cum = pair_add(cum, t);
     }
     int keep = top_k;
     if (top_p < 1.0f) {
-        const unsigned reach = __ballot_sync(kFull, lane < top_k && cum >= (double)top_p);
+        const bool reached = cum.hi > top_p || (cum.hi == top_p && cum.lo >= 0.0f);
+        const unsigned reach = __ballot_sync(kFull, lane < top_k && reached);
         if (reach) keep = __ffs(reach);                        // the entry that reaches top_p is kept
     }
-    const double kept = __shfl_sync(kFull, cum, keep - 1);
+    const fpair kept = {__shfl_sync(kFull, cum.hi, keep - 1), __shfl_sync(kFull, cum.lo, keep - 1)};
+    const fpair out = pair_div(pj, kept);
     idx[m * kWidth + lane] = lane < top_k ? (int32_t)(~(uint32_t)(a & 0xFFFFFFFFull)) : -1;
-    probs[m * kWidth + lane] = lane < keep ? (float)(pj / kept) : 0.0f;
+    probs[m * kWidth + lane] = lane < keep ? out.hi : 0.0f;     // the pair's high part: its value rounded to float
 }
 
 }  // namespace topk
