@@ -24,7 +24,7 @@
 //     networks on shuffles), the chunks' top 32 merged, and the slice's top 32
 //     written to scratch.
 //  4. The last CTA of the row to finish (an acq_rel ticket) merges the S sorted
-//     lists (the top 32 of the union of two sorted lists is the elementwise
+//     lists, each warp a share of them and then a tree over the warps (the top 32 of the union of two sorted lists is the elementwise
 //     maximum of one list and the other reversed, merged bitonically), and one
 //     warp forms the probabilities in float pairs (about 48 bits, rounding like
 //     double ones; an exponential below e^-60 in double):
@@ -112,6 +112,21 @@ __device__ __forceinline__ void load_run(const float* row, int i, int len, bool 
     }
 }
 
+// lists[w] (w < kWarps), each sorted descending: the top 32 of their union, by
+// a tree of merges (kWarps/2, then kWarps/4, ... warps at a time).  Called by
+// every thread of the CTA; every thread gets lists[0][lane] of the result.
+__device__ __forceinline__ uint64_t tree_merge(uint64_t (&lists)[kWarps][32], int warp, int lane) {
+#pragma unroll
+    for (int half = kWarps / 2; half >= 1; half >>= 1) {
+        uint64_t v = 0;
+        if (warp < half) v = warp_merge_desc(umax(lists[warp][lane], lists[warp + half][31 - lane]), lane);
+        __syncthreads();                                      // every list of this level has been read
+        if (warp < half) lists[warp][lane] = v;
+        __syncthreads();
+    }
+    return lists[0][lane];
+}
+
 // cand: [M][S][32] scratch; tickets: [M] counters, zero between launches.
 // idx, probs: [M][32].
 // discard != 0 (logits in the library's own scratch): once the slice is read,
@@ -123,7 +138,6 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restri
                                                         int discard) {
     __shared__ uint64_t buf[kCap];
     __shared__ uint64_t lists[kWarps][32];
-    __shared__ uint64_t bound;
     __shared__ int count, is_last;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the logits come from the preceding kernel
@@ -156,11 +170,10 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restri
         uint64_t a = lists[0][lane];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) a = warp_merge_desc(umax(a, lists[w][31 - lane]), lane);
-        const uint64_t b = __shfl_sync(kFull, a, 31);
-        if (lane == 0) bound = b;
+        if (lane == 31) lists[0][31] = a;
     }
     __syncthreads();
-    const uint64_t lb = bound;
+    const uint64_t lb = lists[0][31];
     // the slice again (the CTA's own recent reads: from L1), candidates at or above the bound
 #pragma unroll
     for (int c = 0; c < kRuns; ++c) {
@@ -233,10 +246,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const float* __restri
     }
     lists[warp][lane] = a;
     __syncthreads();
+    a = tree_merge(lists, warp, lane);
     if (warp != 0) return;
-    a = lists[0][lane];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) a = warp_merge_desc(umax(a, lists[w][31 - lane]), lane);
 
     // lane j holds the rank-j candidate.  Probabilities in float pairs (about
     // 48 significant bits, so they round like double-precision ones):
