@@ -16,7 +16,6 @@
 #include "q4.h"
 #include "q4_generic.cuh"
 #include "q4_tc.cuh"
-#include "q4_mma.cuh"
 #include "q4_tm.cuh"
 #include "q4_glue.cuh"
 #include "q4_topk.cuh"
@@ -89,12 +88,6 @@ constexpr int64_t kTcMaxGroups = 2048;
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mutex;
 
-template <int NT>
-cudaError_t prepare_rk() {
-    return cudaFuncSetAttribute(q4::rk::q4_rk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                q4::rk::smem_bytes());
-}
-
 template <int MT>
 cudaError_t prepare_tc() {
     return cudaFuncSetAttribute(q4::tc::q4_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -144,8 +137,6 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
             if (a == cudaSuccess) a = prepare_tc<4>();
             if (a == cudaSuccess) a = prepare_tc<8>();
             if (a == cudaSuccess) a = prepare_tc<16>();
-            if (a == cudaSuccess) a = prepare_rk<1>();
-            if (a == cudaSuccess) a = prepare_rk<2>();
             if (a == cudaSuccess) a = prepare_tm<1>();
             if (a == cudaSuccess) a = prepare_tm<2>();
             if (a == cudaSuccess) a = prepare_tm<4>();
@@ -163,11 +154,9 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
                 g_encode = reinterpret_cast<EncodeTiledFn>(fn);
             }
             // scratch of the tensor-core kernel, sized for one CTA per SM
-            const size_t pbytes = std::max({q4::tc::partial_floats(d.sm_count), q4::rk::partial_floats(d.sm_count),
-                                            q4::tm::partial_floats(d.sm_count)}) *
+            const size_t pbytes = std::max(q4::tc::partial_floats(d.sm_count), q4::tm::partial_floats(d.sm_count)) *
                                   sizeof(float);
-            const size_t sbytes = std::max({q4::tc::sem_ints(d.sm_count), q4::rk::sem_ints(d.sm_count),
-                                            q4::tm::sem_ints(d.sm_count)}) *
+            const size_t sbytes = std::max(q4::tc::sem_ints(d.sm_count), q4::tm::sem_ints(d.sm_count)) *
                                   sizeof(int);
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
@@ -339,41 +328,6 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
     return Q4_OK;
 }
 
-q4_status launch_rk(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
-                    cudaStream_t stream) {
-    using namespace q4::rk;
-    CUtensorMap map_nib;
-    q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
-                            (uint64_t)K / 2, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (s != Q4_OK) return s;
-    Params p;
-    p.W = static_cast<const uint8_t*>(W);
-    p.x = static_cast<const uint16_t*>(x);
-    p.y = y;
-    p.partials = d.partials;
-    p.sems = d.sems;
-    p.error_word = d.error_word;
-    p.N = N;
-    p.K = K;
-    p.M = M;
-    p.G = (int)(K / 64);
-    p.T = (int)((N + kRowsTile - 1) / kRowsTile);
-    p.U = p.T * (p.G / 2);
-    p.C = p.U < d.sm_count ? p.U : d.sm_count;
-#ifdef Q4_TRACE
-    p.trace = g_trace;
-#endif
-    const dim3 grid((unsigned)p.C), block(kThreads);
-    const size_t smem = (size_t)smem_bytes();
-    cudaError_t e;
-    if (M <= 8)
-        e = launch_pdl(q4_rk_kernel<1>, grid, block, smem, stream, map_nib, p);
-    else
-        e = launch_pdl(q4_rk_kernel<2>, grid, block, smem, stream, map_nib, p);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the register-operand Q4 kernel");
-    return Q4_OK;
-}
-
 // The launch plan depends on N, K and the device only -- never on M -- so a
 // row's result is the same for every M.
 bool use_tc(int64_t N, int64_t K) {
@@ -384,26 +338,12 @@ bool use_tc(int64_t N, int64_t K) {
 
 // The kernel for a (validated) matmul: the tensor-memory kernel for K a
 // multiple of 512, the generic kernel otherwise.
-// developer comparison switch: 1 = two-launch tensor-memory kernel, 2 = register-operand kernel
-int alt_kernel_choice() {
-    static const int alt = [] {
-        const char* v = std::getenv("Q4_ALT_KERNEL");
-        return v ? std::atoi(v) : 0;
-    }();
-    return alt;
-}
-
 // records_ready: the x records of this call are already in the scratch (written by
 // a glue kernel in record mode); only valid when use_tc(N, K).
 q4_status dispatch_matmul(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                           cudaStream_t stream, bool records_ready = false) {
     if (records_ready) return launch_tm(d, x, W, M, N, K, y, stream, true);
-    if (use_tc(N, K)) {
-        const int alt_kernel = alt_kernel_choice();
-        if (alt_kernel == 1 && M <= 16) return launch_tc(d, x, W, M, N, K, y, stream);
-        if (alt_kernel == 2 && M <= 16) return launch_rk(d, x, W, M, N, K, y, stream);
-        return launch_tm(d, x, W, M, N, K, y, stream, false);
-    }
+    if (use_tc(N, K)) return launch_tm(d, x, W, M, N, K, y, stream, false);
     return launch_generic(x, W, M, N, K, y, stream);
 }
 
@@ -726,7 +666,7 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
         if (!last) {
             const q4_layer& Nx = layers[j + 1];
             // the next matmul on the tensor-memory kernel: the glue writes its x records directly
-            records_ready = use_tc(Nx.N, Nx.K) && alt_kernel_choice() == 0;
+            records_ready = use_tc(Nx.N, Nx.K);
             s = launch_glue(yj, M, L.N, Nx.K, L.glue, xbuf, st, records_ready ? info->xt : nullptr, rec_w);
             if (s != Q4_OK) return s;
             xj = xbuf;
