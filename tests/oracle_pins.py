@@ -317,6 +317,32 @@ def pin_glue(o) -> None:
     # gate 30 (silu(30) = 30 to within 3e-12), up 1: constant row -> 1.0
     g = np.concatenate([np.full((1, K), 30.0, np.float32), np.ones((1, K), np.float32)], axis=1)
     assert np.all(o.glue(g, K, 2) == 0x3F80)
+    pin_swiglu_orientation(o)
+
+
+def pin_swiglu_orientation(o) -> None:
+    """Which half of y is the gate.  Row 0: gate = 30 on the first 32 inputs and
+    0 on the last 32; up alternates 1, 2 (and 7 where the gate is 0).  Then
+    v = silu(gate) * up = [30, 60, 30, 60, ..., 0, ..., 0] up to 1e-13 relative,
+    mean square (16*900 + 16*3600) / 64 = 1125, so x = 30/sqrt(1125) = 2/sqrt(5)
+    -> bf16 229/256 = 0x3F65 and 60/sqrt(1125) = 4/sqrt(5) -> 229/128 = 0x3FE5,
+    and exactly 0 where the gate is 0.  Row 1 flips the sign of the odd ups:
+    -2/sqrt(5) -> 0xBF65.  With the halves swapped, v = silu(up) * gate gives
+    silu(1)*30 : silu(2)*30 = 0.731 : 1.762, not 1 : 2, and nonzero values where
+    the gate is 0, so every output differs."""
+    K = 64
+    gate = np.zeros((2, K), np.float32)
+    gate[:, :32] = 30.0
+    up = np.zeros((2, K), np.float32)
+    up[:, 0:32:2] = 1.0
+    up[:, 1:32:2] = 2.0
+    up[:, 32:] = 7.0
+    up[1, 0:32:2] = -1.0
+    x = o.glue(np.concatenate([gate, up], axis=1), K, 2)
+    want0 = np.array([0x3F65, 0x3FE5] * 16 + [0] * 32, dtype=np.uint16)
+    want1 = np.array([0xBF65, 0x3FE5] * 16 + [0] * 32, dtype=np.uint16)
+    assert np.array_equal(x[0], want0), [hex(v) for v in x[0][:4]]
+    assert np.array_equal(x[1], want1), [hex(v) for v in x[1][:4]]
 
 
 ALL_PINS = [pin_packed_bytes, pin_model_totals, pin_one_hot, pin_group_closed_forms,

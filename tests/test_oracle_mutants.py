@@ -1,7 +1,8 @@
 """Plant mistakes in copies of the oracle (on the CPU) and check that the pins
 catch each one: a wrong nibble order, swapped scale/bias planes, a wrong group
 size, a dropped bias, a sign error, weights rounded to bf16, a transposed
-index and a dropped glue term must each fail at least one pin."""
+index, a dropped glue term and swapped gate and up halves must each fail at
+least one pin."""
 import os
 import shutil
 import tempfile
@@ -31,6 +32,8 @@ MUTANTS = {
     "glue_no_gate": ("if (kind == 2) a = a / (1.0 + exp(-a)) * (double)yr[K + k];",
                      "if (kind == 2) a = (double)yr[K + k];"),
     "tie_rounds_up": ("else r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "else r = fl + 1.0;"),
+    "gate_up_swapped": ("if (kind == 2) a = a / (1.0 + exp(-a)) * (double)yr[K + k];",
+                        "if (kind == 2) { double u = (double)yr[K + k]; a = u / (1.0 + exp(-u)) * a; }"),
 }
 
 
