@@ -67,7 +67,9 @@ struct DeviceInfo {
     int sm_count = 0;
     float* partials = nullptr;      // split-K partial sums of the tensor-core kernel
     int* sems = nullptr;            // per-tile arrival counters (zero between launches)
+    size_t sem_bytes = 0;
     uint8_t* xt = nullptr;          // prepared x records (one per group of 64 inputs)
+    unsigned int* ctl = nullptr;    // call counters of the tensor-memory kernel (zero between launches)
     uint64_t* topk_cand = nullptr;  // sampling epilogue: per-slice candidates [16][128][32]
     int* topk_tickets = nullptr;    // sampling epilogue: per-row arrival counters (zero between launches)
     unsigned int* error_word = nullptr;
@@ -158,12 +160,15 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
                                   sizeof(float);
             const size_t sbytes = std::max(q4::tc::sem_ints(d.sm_count), q4::tm::sem_ints(d.sm_count)) *
                                   sizeof(int);
+            d.sem_bytes = sbytes;
             a = cudaMalloc(&d.partials, pbytes);
             if (a == cudaSuccess) a = cudaMalloc(&d.sems, sbytes);
             if (a == cudaSuccess)
                 a = cudaMalloc(&d.xt, (size_t)kTcMaxGroups * std::max(q4::prep::kRecordBytes, q4::tm::rec_bytes(32)));
             if (a == cudaSuccess)
                 a = cudaMalloc(&d.topk_cand, (size_t)Q4_MAX_ROWS * q4::topk::kMaxSlices * q4::topk::kWidth * sizeof(uint64_t));
+            if (a == cudaSuccess) a = cudaMalloc(&d.ctl, q4::tm::kCtlWords * sizeof(unsigned int));
+            if (a == cudaSuccess) a = cudaMemset(d.ctl, 0, q4::tm::kCtlWords * sizeof(unsigned int));
             if (a == cudaSuccess) a = cudaMalloc(&d.topk_tickets, (size_t)Q4_MAX_ROWS * sizeof(int));
             if (a == cudaSuccess) a = cudaMemset(d.topk_tickets, 0, (size_t)Q4_MAX_ROWS * sizeof(int));
             if (a == cudaSuccess) a = cudaMemset(d.sems, 0, sbytes);
@@ -178,6 +183,19 @@ q4_status device_setup(int* dev_out, const DeviceInfo** info_out) {
     *dev_out = dev;
     *info_out = &d;
     return Q4_OK;
+}
+
+// Zero the arrival counters of the current device's scratch, if that device
+// has been set up (nothing to do otherwise).  Synchronous; allocates nothing.
+cudaError_t reset_counters(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready || d.status != Q4_OK) return cudaSuccess;
+    cudaError_t e = cudaMemset(d.sems, 0, d.sem_bytes);
+    if (e == cudaSuccess) e = cudaMemset(d.topk_tickets, 0, (size_t)Q4_MAX_ROWS * sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return e;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -284,16 +302,33 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
 q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     cudaStream_t stream, bool records_ready) {
     using namespace q4::tm;
-    CUtensorMap map_nib;
+    const int MT = tm_rows_template(M);
+    CUtensorMap map_nib, map_sb;
+    const uint8_t* w8 = static_cast<const uint8_t*>(W);
+    const uint64_t G = (uint64_t)K / 64;
     q4_status s = encode_2d(&map_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)K / 2, (uint64_t)N,
                             (uint64_t)K / 2, 64, kRowsTile, CU_TENSOR_MAP_SWIZZLE_64B);
+    // scale and bias planes as one 3-D tensor [2][N][G] of bf16 words; boxes of 8 groups x 128 rows x both planes
+    if (s == Q4_OK) {
+        const cuuint64_t dims[3] = {G, (cuuint64_t)N, 2};
+        const cuuint64_t strides[2] = {G * 2, (cuuint64_t)N * G * 2};
+        const cuuint32_t box[3] = {8, (cuuint32_t)kRowsTile, 2};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        const CUresult r = g_encode(&map_sb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                                    const_cast<uint8_t*>(w8 + (uint64_t)N * (uint64_t)K / 2), dims, strides, box, estr,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) s = fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
     if (s != Q4_OK) return s;
     Params p;
-    p.W = static_cast<const uint8_t*>(W);
+    p.W = w8;
     p.y = y;
+    p.x = static_cast<const uint16_t*>(x);
     p.partials = d.partials;
     p.sems = d.sems;
     p.xt = d.xt;
+    p.ctl = d.ctl;
     p.error_word = d.error_word;
     p.N = N;
     p.K = K;
@@ -302,27 +337,22 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
     p.GP = p.G / 2;
     p.T = (int)((N + kRowsTile - 1) / kRowsTile);
     p.U = p.T * p.GP;
-    p.C = p.U < d.sm_count ? p.U : d.sm_count;
+    p.C = grid_ctas(p.U, d.sm_count);
+    p.R = kTeams * p.C;
+    p.build = records_ready ? 0 : 1;   // else the preceding glue kernel wrote the records
 #ifdef Q4_TRACE
     p.trace = g_trace;
 #endif
-    const int MT = tm_rows_template(M);
     cudaError_t e = cudaSuccess;
-    if (!records_ready)   // else the preceding glue kernel wrote them
-        e = MT <= 16 ? launch_pdl(xrec_kernel<16>, dim3((unsigned)p.G), dim3(8 * 16), 0, stream,
-                                  static_cast<const uint16_t*>(x), M, K, d.xt)
-                     : launch_pdl(xrec_kernel<32>, dim3((unsigned)p.G), dim3(8 * 32), 0, stream,
-                                  static_cast<const uint16_t*>(x), M, K, d.xt);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the x record kernel");
     const dim3 grid((unsigned)p.C), block(kThreads);
     switch (MT) {
-        case 1: e = launch_pdl(q4_tm_kernel<1>, grid, block, (size_t)smem_bytes<1>(), stream, map_nib, p); break;
-        case 2: e = launch_pdl(q4_tm_kernel<2>, grid, block, (size_t)smem_bytes<2>(), stream, map_nib, p); break;
-        case 4: e = launch_pdl(q4_tm_kernel<4>, grid, block, (size_t)smem_bytes<4>(), stream, map_nib, p); break;
-        case 8: e = launch_pdl(q4_tm_kernel<8>, grid, block, (size_t)smem_bytes<8>(), stream, map_nib, p); break;
-        case 16: e = launch_pdl(q4_tm_kernel<16>, grid, block, (size_t)smem_bytes<16>(), stream, map_nib, p); break;
-        case 24: e = launch_pdl(q4_tm_kernel<24>, grid, block, (size_t)smem_bytes<24>(), stream, map_nib, p); break;
-        default: e = launch_pdl(q4_tm_kernel<32>, grid, block, (size_t)smem_bytes<32>(), stream, map_nib, p); break;
+        case 1: e = launch_pdl(q4_tm_kernel<1>, grid, block, (size_t)smem_bytes<1>(), stream, map_nib, map_sb, p); break;
+        case 2: e = launch_pdl(q4_tm_kernel<2>, grid, block, (size_t)smem_bytes<2>(), stream, map_nib, map_sb, p); break;
+        case 4: e = launch_pdl(q4_tm_kernel<4>, grid, block, (size_t)smem_bytes<4>(), stream, map_nib, map_sb, p); break;
+        case 8: e = launch_pdl(q4_tm_kernel<8>, grid, block, (size_t)smem_bytes<8>(), stream, map_nib, map_sb, p); break;
+        case 16: e = launch_pdl(q4_tm_kernel<16>, grid, block, (size_t)smem_bytes<16>(), stream, map_nib, map_sb, p); break;
+        case 24: e = launch_pdl(q4_tm_kernel<24>, grid, block, (size_t)smem_bytes<24>(), stream, map_nib, map_sb, p); break;
+        default: e = launch_pdl(q4_tm_kernel<32>, grid, block, (size_t)smem_bytes<32>(), stream, map_nib, map_sb, p); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the tensor-memory Q4 kernel");
     return Q4_OK;
@@ -342,8 +372,7 @@ bool use_tc(int64_t N, int64_t K) {
 // a glue kernel in record mode); only valid when use_tc(N, K).
 q4_status dispatch_matmul(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                           cudaStream_t stream, bool records_ready = false) {
-    if (records_ready) return launch_tm(d, x, W, M, N, K, y, stream, true);
-    if (use_tc(N, K)) return launch_tm(d, x, W, M, N, K, y, stream, false);
+    if (use_tc(N, K)) return launch_tm(d, x, W, M, N, K, y, stream, records_ready);
     return launch_generic(x, W, M, N, K, y, stream);
 }
 
@@ -446,6 +475,7 @@ constexpr size_t kNoAllocPartialBytes =
 constexpr size_t kNoAllocSemBytes = round256((size_t)kNoAllocMaxSms * q4::tc::kCG * sizeof(int));
 constexpr size_t kNoAllocXtBytes = round256((size_t)(kNoAllocMaxK / 64) * q4::prep::kRecordBytes);
 constexpr size_t kNoAllocScratchBytes = kNoAllocPartialBytes + kNoAllocSemBytes + kNoAllocXtBytes;
+static_assert(kNoAllocScratchBytes == 8542208, "the size q4.h states for q4_matmul_noalloc's scratch");
 
 }  // namespace
 
@@ -812,11 +842,13 @@ q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream) {
 
 q4_status q4_device_status(q4_stream_t stream) {
     g_last_error.clear();
+    // No set-up here: this call allocates nothing, so a caller of
+    // q4_matmul_noalloc can use it too.  It reads the error word through the
+    // symbol of the current device.
     int dev = 0;
-    const DeviceInfo* info = nullptr;
-    q4_status s = device_setup(&dev, &info);
-    if (s != Q4_OK) return s;
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     unsigned int word = 0;
     e = cudaMemcpyFromSymbol(&word, q4_device_error_word, sizeof word);
@@ -825,6 +857,13 @@ q4_status q4_device_status(q4_stream_t stream) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(q4_device_error_word, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (word & ~q4::edges::kErrBadIndex) {
+            // A CTA that gave up a wait skipped its arrivals on the split-K and
+            // top-k counters, which the next launch expects at zero: clear them
+            // (q4_matmul_noalloc clears its own on every call).
+            e = reset_counters(dev);
+            if (e != cudaSuccess) return cuda_fail(e, "clearing the library's arrival counters");
+        }
         if (word & q4::edges::kErrBadIndex)
             return fail(Q4_ERR_INVALID_INDEX, "a codebook id was outside 0..V-1 (error word 0x%x)", word);
         return fail(Q4_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);

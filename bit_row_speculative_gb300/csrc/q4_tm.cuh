@@ -16,58 +16,64 @@
 // costs one shift, four AND and four bf16x2 subtractions.  The x operand
 // carries the inverse powers (x * 2^100 for even inputs, x * 2^96 for odd
 // ones), so every tensor-core product is (q - c) * x * 2^-33 exactly and the
-// fold applies s * 2^33.  (|x| must stay below 2^28 for x * 2^100 to be finite.)
+// fold applies s * 2^33.  Range: |x| < 2^28 (x * 2^100 stays finite); a
+// nonzero |x| below 2^-93 gives products below the fp32 normal range, which
+// the tensor core may flush; s * 2^33 must stay finite (|s| < 2^95).
 //
-// Two kernels per call, chained by programmatic dependent launch:
-//   xrec_kernel  writes each group's x record to global scratch: the fp32
-//                group sums X[0..W-1], then the rows of x for the group's 64
-//                inputs as tensor-core core matrices (8 rows x 8 inputs, 128 B
-//                each), 8-row blocks one after another (2112 bytes at W = 16,
-//                4224 at W = 32; W = 16 for M <= 16, 32 for M <= 32).  Inputs
-//                of each 8-block are in the dequantized order k0 k4 k1 k5 k2
-//                k6 k3 k7 and scaled as above; rows >= M are zero.  A kernel
-//                for M <= 8 copies only the first 1088 bytes (X and rows 0-7).
-//                Inside a chained pass the glue kernel writes the records
-//                instead, and this kernel is not launched.
-//   q4_tm_kernel one persistent CTA per SM, 16 warps; tiles of 128 rows, a
-//                stage is two groups (128 inputs) of one tile.
-//     warp 0       producer: per stage one 128-row x 64-byte nibble box (TMA,
-//                  64-byte swizzle) into a ring of slots, and bulk copies of
-//                  the two x records into the same slot.  The weight boxes of
-//                  the first ring-full of stages are issued before the kernel
-//                  waits for its predecessor (they need nothing from it);
-//                  every record copy comes after that wait.
-//     warps 1..3   MMA issuers, one per team: per stage of the team 8 MMAs
-//                  M128 N=W K16 (A = the dequantized weights in the team's
-//                  tensor memory, B = the x records in shared memory, D = the
-//                  team's P) and a commit to the team's "done" barrier.  Each
-//                  column of an N = 32 MMA carries the same bits as the same
-//                  column of an N = 16 MMA (tested: rows at M = 17..32 equal
-//                  the rows at M <= 16), so row invariance holds across widths.
-//     warps 4..15  three consumer teams of 4 warps; stage i belongs to team
-//                  i % 3.  Every team covers all 128 rows (one row per
-//                  thread).  At W = 16 a team keeps two A buffers: in its
-//                  iteration for stage i it dequantizes stage i into one
-//                  buffer while the MMAs of its previous stage (i - 3) finish
-//                  on the other, then folds that previous stage's P into its
-//                  own fp32 sums with s, r and X, frees that stage's slot and
-//                  hands stage i over.  At W = 32 (one A buffer, to fit tensor
-//                  memory) it folds the previous stage first.  The three teams
-//                  overlap with each other.  At the end of each tile segment
-//                  the teams' sums are added in team order through shared
-//                  memory.
-// The ring has a multiple of 3 slots, so a slot always serves the same team,
-// and every barrier is waited on by threads that pass through its phases in
-// order (a parity wait never sees a phase two steps away).
-// Work split: the T*G/2 (tile, group pair) units are cut into equal contiguous
-// ranges, one per CTA (stream-K).  A tile whose units span several CTAs is
-// finished by the last of them to arrive, which adds the partial sums in
-// increasing CTA order.  The split depends only on N, K and the grid size, and
-// nothing in the arithmetic of row m depends on the other rows, so every
-// row's result is independent of M.
-// No CTA waits for another except through the last-arriver counter, which
-// never blocks.  Every barrier wait is bounded; a wait that runs out sets the
-// error word and the CTA runs to its end without further waiting.
+// x records.  Per group of 64 inputs: the fp32 group sums X[0..W-1], then the
+// rows of x for the group's inputs as tensor-core core matrices (8 rows x 8
+// inputs, 128 B each), 8-row blocks one after another (2112 bytes at W = 16,
+// 4224 at W = 32; W = 16 for M <= 16, 32 for M <= 32).  Inputs of each 8-block
+// are in the dequantized order k0 k4 k1 k5 k2 k6 k3 k7 and scaled as above;
+// rows >= M are zero.  A call builds them into global scratch at its start: the
+// MMA-issuer warps of CTA c build groups c, c + C, ... and count them on a device
+// counter, and a team's producer lanes copy a stage's records only once the
+// count says all are there.  Meanwhile each consumer team builds the records of
+// its own first stages from x straight into its shared record slots, so it can
+// start about one L2 latency after its predecessor finished.  Inside a chained
+// pass the glue kernel has already written the records, and the call neither
+// builds nor waits.
+//
+// One persistent CTA per SM, 16 warps; tiles of 128 rows (tensor-memory
+// lanes), a stage is two groups (128 inputs) of one tile.  The T*G/2 (tile,
+// group pair) units are cut into R = 3C equal contiguous ranges (stream-K),
+// and consumer team j of CTA c works through range 3c + j on its own.
+//   warp 0       producers.  One thread keeps only about one TMA operation in
+//                flight at a time, so each team's streams are spread over
+//                lanes: two issue its weights (a 128-row x 64-byte nibble box
+//                per stage, L2 evict-first, into the team's nibble ring, and
+//                at the first stage of each block of 8 groups a box of those
+//                rows' scale and bias words), two copy its stages' records
+//                into its record ring.  The lanes run one polling loop.
+//   warps 1..3   MMA issuers, one per team: per stage 8 MMAs M128 N16 K16 (16
+//                at W = 32: rows 0-15 and rows 16-31 as two N = 16 MMAs, so a
+//                row's products never depend on the row width), A = the
+//                dequantized weights in the team's tensor memory, B = the
+//                stage's records in shared memory, D = the team's P; then a
+//                commit to the team's "done" barrier.  Before that, their
+//                share of the call's records.
+//   warps 4..15  three consumer teams of 4 warps, one row per thread.  At
+//                W = 16 a team keeps two A buffers: in its iteration for stage
+//                k it dequantizes stage k into one (and frees its nibble slot
+//                at once) while the MMAs of stage k - 1 run on the other,
+//                loads that stage's P, hands stage k to its issuer, then folds
+//                P into its fp32 sums with s, r and X and frees the record
+//                slot.  At W = 32 (one A buffer, to fit tensor memory) it
+//                folds stage k - 1 first.
+// Segment ends: a range covers at most two partial tiles (its first and last
+// segments) and whole tiles between.  A warp stores a whole tile's 32 rows to
+// y; for a partial tile it publishes its rows and counts them on the tile's
+// quarter counter, and the last of the tile's contributors to arrive adds the
+// partials in increasing range order and stores y.  No warp waits for another
+// warp or CTA there.  The split depends only on N, K and the SM count, and
+// nothing in the arithmetic of row m depends on the other rows, so every row's
+// result is independent of M and of the run.
+// Every barrier wait is bounded; a wait that runs out sets the error word and
+// the CTA runs to its end without further waiting.  The last CTA to finish
+// returns the call's counters to zero (and the tile counters too after a
+// timed-out wait), so the next call starts clean.  All CTAs of a call must be
+// resident together (one per SM, as launched): a CTA waits for the records the
+// others build.
 #pragma once
 
 #include <cuda.h>
@@ -80,32 +86,53 @@ namespace tm {
 
 constexpr int kRowsTile = 128;              // rows per tile (tensor-memory lanes)
 constexpr int kTeams = 3;                   // consumer teams (one warpgroup each)
-constexpr int kIssuersPerTeam = 1;          // MMA issuing threads per team (they split the two groups)
-constexpr int kIssuers = kIssuersPerTeam * kTeams;
 constexpr int kConsumerWarp0 = 4;           // warps 4.. (warp % 4 = tensor-memory lane quarter)
 constexpr int kThreads = (kConsumerWarp0 + 4 * kTeams) * 32;   // 512
-constexpr int kConsumerThreads = kTeams * 128;
-static_assert(kIssuers + 1 <= kConsumerWarp0, "control warps");
+constexpr int kNibStage = kRowsTile * 64;   // 8 KB: 128 rows x 64 B (two groups)
+constexpr int kRecHalf = 1088;              // W = 16: X and rows 0-7
 
-// Row width W: the x records and the MMAs cover W = 16 rows for M <= 16 and
-// W = 32 rows for 16 < M <= 32.  Everything of the layout below depends on W.
 template <int MT>
 __host__ __device__ constexpr int width() { return MT > 16 ? 32 : 16; }
 __host__ __device__ constexpr int rec_bytes(int W) { return 4 * W + (W / 8) * 1024; }   // X[W] fp32, then W/8 blocks of 8 rows
 __host__ __device__ constexpr int rec_b(int W) { return 4 * W; }                        // offset of the core matrices
-constexpr int kRecHalf = 1088;                        // W = 16: X and rows 0-7
-constexpr int kNibStage = kRowsTile * 64;             // 8 KB: 128 rows x 64 B (two groups)
-__host__ __device__ constexpr int stage_bytes(int W) { return ((kNibStage + 2 * rec_bytes(W) + 1023) / 1024) * 1024; }
-__host__ __device__ constexpr int stages(int W) { return W == 16 ? 12 : 9; }            // a multiple of kTeams
-// team sums of a segment: two buffers used alternately at W = 16, one at W = 32
-__host__ __device__ constexpr int red_buffers(int W) { return W == 16 ? 2 : 1; }
-__host__ __device__ constexpr int red_bytes(int W) { return red_buffers(W) * kTeams * W * kRowsTile * 4; }
+// Per team: a ring of nibble slots (one 128-row x 64-byte box each, freed as
+// soon as a stage is dequantized) and a ring of record slots (the stage's two x
+// records, freed once its P is folded; the group sums X in them are read by all
+// four warps of the team).
+__host__ __device__ constexpr int nib_slots(int W) { return W == 16 ? 5 : 4; }
+__host__ __device__ constexpr int rec_slots(int W) { return W == 16 ? 6 : 4; }
+__host__ __device__ constexpr int rec_stage_bytes(int W) { return ((2 * rec_bytes(W) + 127) / 128) * 128; }
+// Stages whose records a team builds itself from x at its start (they do not
+// wait for the call's shared records).
+__host__ __device__ constexpr int local_stages(int W) { return W == 16 ? 3 : 2; }
+// Producer lanes per team and stream.  A lane issues every L-th stage of its
+// team into a ring of S slots and waits, by phase parity, for the slot's previous
+// user; that wait is unambiguous only while the lane cannot run more than one
+// phase ahead of the slot, which L <= S guarantees (its own previous stage, L
+// earlier, already waited for the stage S before that).
+constexpr int kWeightLanes = 2;
+constexpr int kRecordLanes = 2;
+// Scale and bias words: per team two buffers (blocks of 8 groups = 4 stages),
+// each a 128-row x 16-byte box of the scale plane and one of the bias plane.  A
+// buffer is reloaded at the first stage of the block after next, which the
+// producer issues only once the nibble slot of the stage nib_slots earlier has
+// been freed: at most 5 slots keep that stage at or after the last stage of the
+// block the buffer held.
+constexpr int kSbBuffers = 2;
+constexpr int kSbBox = kRowsTile * 16;                          // 2 KB
+constexpr int kSbBytes = kTeams * kSbBuffers * 2 * kSbBox;      // 24 KB
+static_assert(nib_slots(16) <= 4 * (kSbBuffers - 1) + 1 && nib_slots(32) <= 4 * (kSbBuffers - 1) + 1,
+              "a scale/bias buffer could be reloaded while a stage of its block is still unread");
 constexpr int kBarrierBytes = 1024;
 __host__ __device__ constexpr int smem_bytes_w(int W) {
-    return stages(W) * stage_bytes(W) + red_bytes(W) + kBarrierBytes + 1024 /* alignment slack */;
+    return kTeams * (nib_slots(W) * kNibStage + rec_slots(W) * rec_stage_bytes(W)) + kSbBytes + kBarrierBytes +
+           1024 /* alignment slack */;
 }
-static_assert(stages(16) % kTeams == 0 && stages(32) % kTeams == 0, "each ring slot must belong to one team");
 static_assert(smem_bytes_w(16) <= 232448 && smem_bytes_w(32) <= 232448, "shared memory per CTA");
+static_assert(kWeightLanes <= nib_slots(16) && kWeightLanes <= nib_slots(32) && kRecordLanes <= rec_slots(16) &&
+                  kRecordLanes <= rec_slots(32),
+              "a producer lane could wait on a slot two phases ahead");
+static_assert(local_stages(16) <= rec_slots(16) && local_stages(32) <= rec_slots(32), "local stages fit the ring");
 
 // tensor-memory columns per team: the dequantized A of a stage (two groups x
 // 32), twice at W = 16 (double-buffered), once at W = 32; then P (two groups x W)
@@ -122,58 +149,71 @@ constexpr float kFoldScale = 8589934592.0f;        // 2^33: undoes 2^-133 (weigh
 constexpr uint32_t kXScaleEven = 0x71807180u;      // bf16 pair (2^100, 2^100)
 constexpr uint32_t kXScaleOdd = 0x6F806F80u;       // bf16 pair (2^96, 2^96)
 
+// Error-word codes of this kernel (a wait that ran out, by role).
+constexpr unsigned kErrProducer = 1u, kErrIssuer = 2u, kErrConsumer = 4u, kErrRecords = 8u;
+
+// Call counters in scratch (zero between launches).
+constexpr int kCtlBuilt = 0;     // shared x records built in this call
+constexpr int kCtlDone = 1;      // CTAs finished
+constexpr int kCtlAbort = 2;     // some CTA gave up a wait
+constexpr int kCtlWords = 4;
+
 struct Params {
     const uint8_t* W;           // packed weights
     float* y;                   // [M, N]
-    float* partials;            // scratch: [C][2][W][128]
-    int* sems;                  // scratch: [C], zero between launches
-    const uint8_t* xt;          // x records [G][rec_bytes(W)] (written by xrec_kernel)
+    const uint16_t* x;          // bf16 [M, K]
+    float* partials;            // scratch: [R][2][W][128]
+    int* sems;                  // scratch: [R][4] tile-quarter counters, zero between launches
+    uint8_t* xt;                // scratch: the call's x records [G][rec_bytes(W)]
+    unsigned int* ctl;          // scratch: call counters [kCtlWords], zero between launches
     unsigned int* error_word;   // set on a timed-out wait
     int64_t N;
     int64_t K;
     int M;
-    int G;                      // K / 64 (a multiple of 8)
+    int G;                      // K / 64
     int GP;                     // G / 2 group pairs (stages per tile)
     int T;                      // tiles of 128 rows
     int U;                      // T * GP units
     int C;                      // CTAs (grid size)
+    int R;                      // 3 * C ranges
+    int build;                  // 1: build the x records here; 0: the preceding glue kernel wrote them
 #ifdef Q4_TRACE
     unsigned long long* trace;  // developer timing trace (compiled in only with Q4_TRACE)
 #endif
 };
 
 #ifdef Q4_TRACE
-#define Q4_TMTR(p, idx)                                                                   \
-    do {                                                                                  \
-        if ((p).trace && blockIdx.x == 0 && (idx) < 4096) (p).trace[(idx)] = clock64(); \
-    } while (0)
-// globaltimer (ns) of any CTA, for start/end skew across CTAs
-#define Q4_TMGT(p, idx)                                                                  \
+// globaltimer (ns) of event `ev` (0..15) of CTA c; slots 16..31 hold counters
+#define Q4_TMGT(p, c, ev)                                                                \
     do {                                                                                 \
-        if ((p).trace && (idx) < 4096) {                                                 \
+        if ((p).trace) {                                                                 \
             unsigned long long gt_;                                                      \
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(gt_));                      \
-            (p).trace[(idx)] = gt_;                                                      \
+            (p).trace[(c) * 32 + (ev)] = gt_;                                            \
         }                                                                                \
     } while (0)
 #else
-#define Q4_TMTR(p, idx) \
-    do {                \
-    } while (0)
-#define Q4_TMGT(p, idx) \
-    do {                \
+#define Q4_TMGT(p, c, ev) \
+    do {                  \
     } while (0)
 #endif
 
-// Range of units owned by CTA c.
-__device__ __forceinline__ int range_start(int U, int C, int c) { return (int)(((int64_t)U * c) / C); }
+// Launch geometry: grid and range count from the unit count and the SM count only.
+inline int grid_ctas(int U, int sm_count) {
+    int c = U / kTeams;
+    if (c < 1) c = 1;
+    return c < sm_count ? c : sm_count;
+}
 
-// CTA that owns unit u.
-__device__ __forceinline__ int cta_of_unit(int U, int C, int u) {
-    int c = (int)(((int64_t)u * C) / U);
-    while (c + 1 < C && range_start(U, C, c + 1) <= u) ++c;
-    while (c > 0 && range_start(U, C, c) > u) --c;
-    return c;
+// First unit of range r.
+__host__ __device__ __forceinline__ int range_start(int U, int R, int r) { return (int)(((int64_t)U * r) / R); }
+
+// The (non-empty) range that owns unit u: the largest r with range_start(r) <= u.
+__device__ __forceinline__ int range_of_unit(int U, int R, int u) {
+    int r = (int)(((int64_t)u * R) / U);
+    while (r + 1 < R && range_start(U, R, r + 1) <= u) ++r;
+    while (r > 0 && range_start(U, R, r) > u) --r;
+    return r;
 }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -212,6 +252,18 @@ __device__ __forceinline__ void fma2(float& acc0, float& acc1, float a, float b0
     acc1 = __uint_as_float((uint32_t)(d >> 32));
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -219,46 +271,82 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void record_timeout(const Params& p, unsigned int code, volatile int* abort_flag) {
     *abort_flag = 1;
     atomicOr(p.error_word, code);
 }
 
+#ifdef Q4_TRACE
+__device__ unsigned long long q4_tm_spins[2];   // developer counters: wait-loop iterations
+#endif
+
 // Bounded wait that also gives up at once when another role has already
 // given up (the whole CTA then runs to its end without further waiting).
 __device__ __forceinline__ bool wait_or_abort(const Params& p, uint64_t* bar, uint32_t parity, unsigned code,
-                                              volatile int* abort_flag) {
+                                              volatile int* abort_flag, unsigned long long* spins = nullptr) {
     if (q4::sm100::mbar_try_wait(bar, parity)) return true;       // fast path: already complete
     if (*abort_flag) return false;
-    if (q4::sm100::mbar_wait(bar, parity, kWaitLimit)) return true;
-    record_timeout(p, code, abort_flag);
-    return false;
+#ifdef Q4_TRACE
+    if (spins) {
+        const long long t0 = clock64();
+        unsigned long long n = 0;
+        bool ok = true;
+        while (!q4::sm100::mbar_try_wait_sleep(bar, parity, 20000u)) {
+            ++n;
+            if (clock64() - t0 > kWaitLimit) {
+                ok = false;
+                break;
+            }
+        }
+        *spins += n + 1;
+        if (ok) return true;
+        record_timeout(p, code, abort_flag);
+        return false;
+    }
+#else
+    (void)spins;
+#endif
+    // suspended in the hardware between checks; another role's abort ends the wait too
+    const long long t0 = clock64();
+    while (!q4::sm100::mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            record_timeout(p, code, abort_flag);
+            return false;
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ x records
-// One CTA per group of 64 inputs, 8 * W threads: thread t takes row m = t / 8
-// and 8-block kc = t % 8 of the group.
-template <int W>
-__global__ void __launch_bounds__(8 * W) xrec_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
-                                                     uint8_t* __restrict__ xt) {
-    pdl_launch_dependents();
-    // x may come from the preceding kernel, and the preceding matmul may still
-    // read the records of its own call: wait for it first
-    pdl_wait();
-    const int g = blockIdx.x;
-    const int t = threadIdx.x;
-    const int m = t >> 3, kc = t & 7;
+// One item of a record: row m, 8-block kc of group g.  record_load fetches its
+// 8 inputs (zero for rows past M); record_item permutes them to the dequantized
+// order and scales them (o), and forms the row's group sum X over the 8 blocks (in
+// 8 consecutive lanes, kc = lane % 8: the 8 inputs in increasing k, then a fixed
+// xor tree) -- the same operations for every M.  All 32 lanes call record_item.
+__device__ __forceinline__ uint4 record_load(const uint16_t* __restrict__ x, int M, int64_t K, int g, int m, int kc) {
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (m < M) v = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)m * K + (int64_t)g * 64 + kc * 8));
-    uint4 o;
+    if (m < M) v = __ldcg(reinterpret_cast<const uint4*>(x + (int64_t)m * K + (int64_t)g * 64 + kc * 8));
+    return v;
+}
+
+__device__ __forceinline__ void record_item(const uint4& v, uint4& o, float& X) {
     o.x = bf16x2_mul(prmt(v.x, v.z, 0x5410u), kXScaleEven);    // (k0, k4)
     o.y = bf16x2_mul(prmt(v.x, v.z, 0x7632u), kXScaleOdd);     // (k1, k5)
     o.z = bf16x2_mul(prmt(v.y, v.w, 0x5410u), kXScaleEven);    // (k2, k6)
     o.w = bf16x2_mul(prmt(v.y, v.w, 0x7632u), kXScaleOdd);     // (k3, k7)
-    uint8_t* rec = xt + (int64_t)g * rec_bytes(W);
-    *reinterpret_cast<uint4*>(rec + rec_b(W) + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
-    // X: the 8 inputs in increasing k, then the 8 block sums of the row (in 8
-    // consecutive lanes) by a fixed xor tree
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float s = 0.0f;
 #pragma unroll
@@ -269,29 +357,118 @@ __global__ void __launch_bounds__(8 * W) xrec_kernel(const uint16_t* __restrict_
     s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
     s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
     s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 4));
-    if (kc == 0) reinterpret_cast<float*>(rec)[m] = s;
+    X = s;
+}
+
+// Byte offset of item (m, kc) in a record.
+template <int W>
+__device__ __forceinline__ int record_item_offset(int m, int kc) { return rec_b(W) + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16; }
+
+// Group g's record into global scratch by one warp (W/4 passes of 4 rows, every
+// load in flight together).
+template <int W>
+__device__ __forceinline__ void build_record_global(const uint16_t* __restrict__ x, int M, int64_t K, int g, int lane,
+                                                    uint8_t* __restrict__ xt) {
+    uint8_t* rec = xt + (int64_t)g * rec_bytes(W);
+    const int kc = lane & 7;
+    uint4 v[W / 4];
+#pragma unroll
+    for (int pass = 0; pass < W / 4; ++pass) v[pass] = record_load(x, M, K, g, (lane >> 3) + 4 * pass, kc);
+#pragma unroll
+    for (int pass = 0; pass < W / 4; ++pass) {
+        const int m = (lane >> 3) + 4 * pass;
+        uint4 o;
+        float X;
+        record_item(v[pass], o, X);
+        *reinterpret_cast<uint4*>(rec + record_item_offset<W>(m, kc)) = o;
+        if (kc == 0) reinterpret_cast<float*>(rec)[m] = X;
+    }
+}
+
+// The records of NS consecutive stages (group pairs gp0, gp0 + 1, ... wrapping
+// at GP) into shared record slots, by a team's 128 threads (thread t: rows t / 8
+// (+ 16 at W = 32), 8-block t % 8, both groups), every load in flight together.
+// slot(i): shared address of stage i's record slot.
+template <int W, int NS, typename SlotFn>
+__device__ __forceinline__ void build_records_smem(const uint16_t* __restrict__ x, int M, int64_t K, int gp0, int GP,
+                                                   int n, int t, SlotFn slot) {
+    const int kc = t & 7;
+    uint4 v[NS][2][W / 16];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int gp = (gp0 + i) % GP;
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int h = 0; h < W / 16; ++h)
+                v[i][g][h] = i < n ? record_load(x, M, K, 2 * gp + g, (t >> 3) + 16 * h, kc) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        if (i >= n) break;
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int h = 0; h < W / 16; ++h) {
+                const int m = (t >> 3) + 16 * h;
+                uint4 o;
+                float X;
+                record_item(v[i][g][h], o, X);
+                const uint32_t r = slot(i) + (uint32_t)(g * rec_bytes(W));
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(r + (uint32_t)record_item_offset<W>(m, kc)),
+                             "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                             : "memory");
+                if (kc == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(r + (uint32_t)(4 * m)), "f"(X) : "memory");
+            }
+    }
 }
 
 // Dequantize the 64 nibbles of one row and group (two 16-byte chunks) into 32
 // bf16 pairs, (q - c) * 2^-133 for the even inputs and (q - c) * 2^-129 for the
-// odd ones, word order (k0,k4) (k1,k5) (k2,k6) (k3,k7) per 8 inputs.
+// odd ones, word order (k0,k4) (k1,k5) (k2,k6) (k3,k7) per 8 inputs, and store
+// them to tensor-memory columns taddr .. taddr + 31 of the thread's lane.  Each
+// block of two nibble words (8 columns) is one PTX sequence -- shift, AND, bf16x2
+// subtraction, store -- so its 8 results are formed in the store's registers.
 // cc0 = c * 0x00010001 (c * 2^-133 as a bf16 pair), cc1 = cc0 << 4.
-__device__ __forceinline__ void dequant64(const uint4& n0, const uint4& n1, uint32_t cc0, uint32_t (&a)[32]) {
-    const uint32_t cc1 = cc0 << 4;
-    const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-#pragma unroll
-    for (int wi = 0; wi < 8; ++wi) {
-        const uint32_t v = wv[wi], u = v >> 8;
-        a[4 * wi + 0] = bf16x2_sub(and32(v, 0x000F000Fu), cc0);
-        a[4 * wi + 1] = bf16x2_sub(and32(v, 0x00F000F0u), cc1);
-        a[4 * wi + 2] = bf16x2_sub(and32(u, 0x000F000Fu), cc0);
-        a[4 * wi + 3] = bf16x2_sub(and32(u, 0x00F000F0u), cc1);
-    }
+__device__ __forceinline__ void dequant16_store(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t cc0, uint32_t cc1) {
+    asm volatile(
+        "{\n\t"
+        ".reg .b32 u0, u1, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
+        "shr.b32 u0, %1, 8;\n\t"
+        "shr.b32 u1, %2, 8;\n\t"
+        "and.b32 a0, %1, 0x000F000F;\n\t"
+        "and.b32 a1, %1, 0x00F000F0;\n\t"
+        "and.b32 a2, u0, 0x000F000F;\n\t"
+        "and.b32 a3, u0, 0x00F000F0;\n\t"
+        "and.b32 a4, %2, 0x000F000F;\n\t"
+        "and.b32 a5, %2, 0x00F000F0;\n\t"
+        "and.b32 a6, u1, 0x000F000F;\n\t"
+        "and.b32 a7, u1, 0x00F000F0;\n\t"
+        "sub.rn.bf16x2 a0, a0, %3;\n\t"
+        "sub.rn.bf16x2 a1, a1, %4;\n\t"
+        "sub.rn.bf16x2 a2, a2, %3;\n\t"
+        "sub.rn.bf16x2 a3, a3, %4;\n\t"
+        "sub.rn.bf16x2 a4, a4, %3;\n\t"
+        "sub.rn.bf16x2 a5, a5, %4;\n\t"
+        "sub.rn.bf16x2 a6, a6, %3;\n\t"
+        "sub.rn.bf16x2 a7, a7, %4;\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {a0, a1, a2, a3, a4, a5, a6, a7};\n\t"
+        "}" ::"r"(taddr),
+        "r"(v0), "r"(v1), "r"(cc0), "r"(cc1)
+        : "memory");
 }
 
-// Constants of one row and group from its bf16 scale and bias:
-// c = clamp(rint(-b/s), 0, 15) (NaN -> 0), r = b + c*s, s * 2^33 and the bf16
-// pair c * 2^-133.
+__device__ __forceinline__ void dequant64_store(const uint4& n0, const uint4& n1, uint32_t cc0, uint32_t taddr) {
+    const uint32_t cc1 = cc0 << 4;
+    dequant16_store(taddr, n0.x, n0.y, cc0, cc1);
+    dequant16_store(taddr + 8u, n0.z, n0.w, cc0, cc1);
+    dequant16_store(taddr + 16u, n1.x, n1.y, cc0, cc1);
+    dequant16_store(taddr + 24u, n1.z, n1.w, cc0, cc1);
+}
+
+// Constants of one row and group from its bf16 scale and bias (the low 16
+// bits of s_bits / b_bits): c = clamp(rint(-b/s), 0, 15) (NaN -> 0),
+// r = b + c*s, s * 2^33 and the bf16 pair c * 2^-133.
 __device__ __forceinline__ void group_constants(uint32_t s_bits, uint32_t b_bits, float& s_fold, float& r,
                                                 uint32_t& cc0) {
     const float s = __uint_as_float(s_bits << 16);
@@ -304,155 +481,146 @@ __device__ __forceinline__ void group_constants(uint32_t s_bits, uint32_t b_bits
     cc0 = ci * 0x00010001u;
 }
 
+// acc[m] = fma(s, P[m], fma(r, X[m], acc[m])) for m < MT, the same two
+// roundings in the same order for every MT.  X[m] are the record's fp32 group
+// sums at shared address xs.
 template <int MT>
-__device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, const float* xs, float s, float r) {
+__device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, uint32_t xs, float s, float r) {
     if (MT == 1) {
-        acc[0] = __fmaf_rn(s, __uint_as_float(P[0]), __fmaf_rn(r, xs[0], acc[0]));
+        acc[0] = __fmaf_rn(s, __uint_as_float(P[0]), __fmaf_rn(r, __uint_as_float(lds32(xs)), acc[0]));
+    } else if (MT == 2) {
+        const float x0 = __uint_as_float(lds32(xs)), x1 = __uint_as_float(lds32(xs + 4));
+        fma2(acc[0], acc[1], r, x0, x1);
+        fma2(acc[0], acc[1], s, __uint_as_float(P[0]), __uint_as_float(P[1]));
     } else {
 #pragma unroll
-        for (int m4 = 0; m4 < (MT + 3) / 4; ++m4) {
-            float X[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (MT >= 4) {
-                const float4 v = reinterpret_cast<const float4*>(xs)[m4];
-                X[0] = v.x;
-                X[1] = v.y;
-                X[2] = v.z;
-                X[3] = v.w;
-            } else {
-                X[0] = xs[0];
-                X[1] = xs[1];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-                const int m = 4 * m4 + i;
-                if (m < MT) {
-                    fma2(acc[m], acc[m + 1], r, X[i], X[i + 1]);
-                    fma2(acc[m], acc[m + 1], s, __uint_as_float(P[m]), __uint_as_float(P[m + 1]));
-                }
-            }
+        for (int m4 = 0; m4 < MT / 4; ++m4) {
+            const uint4 v = lds128(xs + 16 * m4);
+            const int m = 4 * m4;
+            fma2(acc[m], acc[m + 1], r, __uint_as_float(v.x), __uint_as_float(v.y));
+            fma2(acc[m], acc[m + 1], s, __uint_as_float(P[m]), __uint_as_float(P[m + 1]));
+            fma2(acc[m + 2], acc[m + 3], r, __uint_as_float(v.z), __uint_as_float(v.w));
+            fma2(acc[m + 2], acc[m + 3], s, __uint_as_float(P[m + 2]), __uint_as_float(P[m + 3]));
         }
     }
 }
 
-// End of a tile segment: the teams' sums of rows [t*128, t*128+128) are added
-// in team order; a whole tile is stored, a partial one published and finished
-// by the last CTA to arrive (partials added in increasing CTA order).  Called
-// by all consumer threads; thread (team, row) handles m = team + kTeams*j.
+// The last contributor to a partial tile: add the partials of every
+// contributing range in increasing range order and store the warp's 32 rows of
+// y.  Kept out of line (rare); it takes no reference to the caller's sums.
 template <int MT>
-__device__ void end_segment(const Params& p, float (&acc)[MT], float* red, int t, bool whole, int slot, int team,
-                            int row, int c_id, int* bcast, bool live) {
-    // red: this segment's buffer (at W = 16 the caller alternates two by segment)
+__device__ __noinline__ void finish_tile(const float* __restrict__ partials, float* __restrict__ y, int64_t N, int M,
+                                         int U, int R, int GP, int t, int row, int r_first, int r_last) {
     constexpr int W = width<MT>();
-    constexpr int kJ = (MT + kTeams - 1) / kTeams;
-#pragma unroll
-    for (int m = 0; m < MT; ++m) red[(team * W + m) * kRowsTile + row] = acc[m];
-    named_barrier(1, kConsumerThreads);
     const int64_t n = (int64_t)t * kRowsTile + row;
-    float v[kJ];
+    float v[MT];
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-        const int m = team + kTeams * j;
-        v[j] = 0.0f;
-        if (m < MT) {
+    for (int m = 0; m < MT; ++m) v[m] = 0.0f;
+    // ranges in increasing order, kB at a time with their loads in flight together
+    constexpr int kB = MT <= 8 ? 4 : (MT <= 16 ? 2 : 1);
+    for (int rb = r_first; rb <= r_last; rb += kB) {
+        float pv[kB][MT];
 #pragma unroll
-            for (int tm_ = 0; tm_ < kTeams; ++tm_) v[j] = __fadd_rn(v[j], red[(tm_ * W + m) * kRowsTile + row]);
+        for (int i = 0; i < kB; ++i) {
+            const int rr = rb + i;
+            const int rs = range_start(U, R, rr);
+            const bool use = rr <= r_last && rs < range_start(U, R, rr + 1);
+            const int cslot = (rs / GP == t) ? 0 : 1;   // the tile is rr's first segment, or its last
+            const float* src = partials + (((int64_t)rr * 2 + cslot) * W) * kRowsTile + row;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) pv[i][m] = use ? __ldcg(src + m * kRowsTile) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < kB; ++i) {
+            if (rb + i > r_last) break;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) v[m] = __fadd_rn(v[m], pv[i][m]);
         }
     }
-    // one buffer: every thread has read it before any thread writes it for the next segment
-    if (red_buffers(W) == 1) named_barrier(1, kConsumerThreads);
+    if (n < N) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (m < M) y[(int64_t)m * N + n] = v[m];
+    }
+}
+
+// End of a tile segment for one warp (32 rows of tile t).  A whole tile goes
+// straight to y.  A partial one is published in the range's slot (0: the
+// range's first segment, 1: its last) and counted on the tile's quarter
+// counter; the last contributor to arrive finishes the tile.  Warp-uniform
+// arguments.
+template <int MT>
+__device__ __forceinline__ void end_segment(const Params& p, float (&acc)[MT], int t, bool whole, int slot, int r,
+                                            int q, int lane, bool live) {
+    constexpr int W = width<MT>();
+    const int row = q * 32 + lane;
+    const int64_t n = (int64_t)t * kRowsTile + row;
     if (whole) {
         if (live && n < p.N) {
 #pragma unroll
-            for (int j = 0; j < kJ; ++j) {
-                const int m = team + kTeams * j;
-                if (m < MT && m < p.M) p.y[(int64_t)m * p.N + n] = v[j];
-            }
+            for (int m = 0; m < MT; ++m)
+                if (m < p.M) p.y[(int64_t)m * p.N + n] = acc[m];
         }
-    } else {
-        float* dst = p.partials + (((int64_t)c_id * 2 + slot) * W) * kRowsTile + row;
-        if (live) {
+    } else if (live) {
+        float* dst = p.partials + (((int64_t)r * 2 + slot) * W) * kRowsTile + row;
 #pragma unroll
-            for (int j = 0; j < kJ; ++j) {
-                const int m = team + kTeams * j;
-                if (m < MT) __stcg(dst + m * kRowsTile, v[j]);
-            }
-        }
-        // the barrier orders every consumer thread's partial stores before
-        // thread 0's release (acq_rel) increment of the tile counter; the last
-        // contributor's acquire, followed by the next barrier, orders the other
-        // CTAs' partials before every thread's reads below
-        named_barrier(1, kConsumerThreads);
+        for (int m = 0; m < MT; ++m) __stcg(dst + m * kRowsTile, acc[m]);
+        // the warp barrier orders every lane's partial stores before lane 0's
+        // release (acq_rel) increment; the last contributor's acquire, followed
+        // by the next warp barrier, orders the other ranges' partials before
+        // every lane's reads in finish_tile
+        __syncwarp();
         const int tu = t * p.GP;
-        const int c_first = cta_of_unit(p.U, p.C, tu);
-        const int c_last = cta_of_unit(p.U, p.C, tu + p.GP - 1);
-        if (team == 0 && row == 0) {
-            int last = 0;
-            if (live) {
-                int* sem = p.sems + c_first;
-                int old;
-                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(sem) : "memory");
-                if (old == c_last - c_first) {
-                    asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(sem) : "memory");   // zero for the next launch
-                    last = 1;
-                }
-            }
-            *bcast = last;
-        }
-        named_barrier(1, kConsumerThreads);
-        if (*bcast) {
-#pragma unroll
-            for (int j = 0; j < kJ; ++j) v[j] = 0.0f;
-            for (int c = c_first; c <= c_last; ++c) {
-                const int cs = range_start(p.U, p.C, c);
-                const int cslot = (cs / p.GP == t) ? 0 : 1;   // the tile is c's first segment, or its last
-                const float* src = p.partials + (((int64_t)c * 2 + cslot) * W) * kRowsTile + row;
-#pragma unroll
-                for (int j = 0; j < kJ; ++j) {
-                    const int m = team + kTeams * j;
-                    if (m < MT) v[j] = __fadd_rn(v[j], __ldcg(src + m * kRowsTile));
-                }
-            }
-            if (n < p.N) {
-#pragma unroll
-                for (int j = 0; j < kJ; ++j) {
-                    const int m = team + kTeams * j;
-                    if (m < MT && m < p.M) p.y[(int64_t)m * p.N + n] = v[j];
-                }
+        const int r_first = range_of_unit(p.U, p.R, tu);
+        const int r_last = range_of_unit(p.U, p.R, tu + p.GP - 1);
+        int count = 0;                                 // non-empty ranges contributing to tile t
+        for (int rr = r_first; rr <= r_last; ++rr)
+            count += range_start(p.U, p.R, rr) < range_start(p.U, p.R, rr + 1) ? 1 : 0;
+        int last = 0;
+        if (lane == 0) {
+            int* sem = p.sems + r_first * 4 + q;
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(sem) : "memory");
+            if (old == count - 1) {
+                asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(sem) : "memory");   // zero for the next launch
+                last = 1;
             }
         }
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        __syncwarp();
+        if (last) finish_tile<MT>(p.partials, p.y, p.N, p.M, p.U, p.R, p.GP, t, row, r_first, r_last);
     }
-    // At W = 16 red alternates between two buffers by segment, so a buffer is
-    // rewritten only after every thread has passed the first barrier of the
-    // segment between (and with it finished reading here); at W = 32 the
-    // barrier after the reads above does that.  bcast is written only on the
-    // partial path, between two barriers
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 }
 
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
-q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
+q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant__ CUtensorMap map_sb, const Params p) {
     using namespace q4::sm100;
     constexpr int W = width<MT>();
-    constexpr int kStages = stages(W);
-    constexpr int kStageBytes = stage_bytes(W);
+    constexpr int SN = nib_slots(W);
+    constexpr int SR = rec_slots(W);
     constexpr int kRec = rec_bytes(W);
     constexpr int kRecB = rec_b(W);
-    constexpr int kRedBytes = red_bytes(W);
+    constexpr int kRecStage = rec_stage_bytes(W);
+    constexpr int H = local_stages(W);
     constexpr uint32_t kColP = col_p(W);
     constexpr uint32_t kColsTeam = cols_team(W);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kRedBytes);   // nibbles and records landed
-    uint64_t* empty = full + kStages;                  // slot free: the owning team has folded it
-    uint64_t* ready = empty + kStages;                 // [kTeams]: the team's A of a stage stored, its P free
-    uint64_t* done = ready + kTeams;                   // [kTeams]: the team's MMAs of a stage complete
-    uint64_t* fin = done + kTeams;                     // [kIssuers]
-    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kIssuers);
+    uint8_t* nib = smem;                                      // [team][SN] nibble boxes
+    uint8_t* rec = nib + kTeams * SN * kNibStage;             // [team][SR] two x records each
+    uint8_t* sb = rec + kTeams * SR * kRecStage;              // [team][kSbBuffers][plane] scale/bias boxes
+    uint64_t* fulln = reinterpret_cast<uint64_t*>(sb + kSbBytes);   // nibbles (+ scale/bias) landed
+    uint64_t* emptyn = fulln + kTeams * SN;                   // nibble slot read (dequantized)
+    uint64_t* fullr = emptyn + kTeams * SN;                   // records landed
+    uint64_t* emptyr = fullr + kTeams * SR;                   // record slot read (MMAs done, P folded)
+    uint64_t* ready = emptyr + kTeams * SR;                   // [kTeams]: the team's A of a stage stored, its P free
+    uint64_t* done = ready + kTeams;                          // [kTeams]: the team's MMAs of a stage complete
+    uint64_t* fin = done + kTeams;                            // [kTeams]
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kTeams);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
-    int* bcast = const_cast<int*>(abort_flag) + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -461,22 +629,20 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
     // the next kernel on the stream may start now
     pdl_launch_dependents();
 
-    // This CTA's units (= stages) [u0, u1): unit u is group pair u % GP of tile u / GP.
-    const int u0 = range_start(p.U, p.C, c_id);
-    const int u1 = range_start(p.U, p.C, c_id + 1);
-    const int nst = u1 - u0;
-    const int t0 = u0 / p.GP, gp0 = u0 - t0 * p.GP;
-
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 2);
-            mbar_init(&empty[s], 4);
+        for (int i = 0; i < kTeams * SN; ++i) {
+            mbar_init(&fulln[i], 1);
+            mbar_init(&emptyn[i], 4);
+        }
+        for (int i = 0; i < kTeams * SR; ++i) {
+            mbar_init(&fullr[i], 1);
+            mbar_init(&emptyr[i], 4);
         }
         for (int i = 0; i < kTeams; ++i) {
             mbar_init(&ready[i], 4);
-            mbar_init(&done[i], kIssuersPerTeam);
+            mbar_init(&done[i], 1);
+            mbar_init(&fin[i], 1);
         }
-        for (int i = 0; i < kIssuers; ++i) mbar_init(&fin[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -484,206 +650,241 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
         tmem_alloc(tmem_base_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) prefetch_tensormap(&map_nib);
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_nib);
+        prefetch_tensormap(&map_sb);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_slot;
-    if (threadIdx.x == 0) {
-        Q4_TMTR(p, 4000);
-        Q4_TMGT(p, 2400 + 8 * c_id);
-    }
+    if (threadIdx.x == 0) Q4_TMGT(p, c_id, 0);
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            int tn = t0, gn = gp0;                     // tile and group pair of the next nibble load
-            // one barrier per stage, two arrivals: the nibble box and the x records, each with its bytes
-            auto issue_nibbles = [&](int slot) {
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)kNibStage);
-                tma_load_2d_hint(smem + slot * kStageBytes, &map_nib, &full[slot], gn * 64, tn * kRowsTile, pol);
-                if (++gn == p.GP) {
-                    gn = 0;
-                    ++tn;
+        // ------------------------------------------------------------ producers
+        // One thread keeps only about one TMA operation in flight at a time, so the
+        // streams are spread over 12 lanes of this warp: kWeightLanes per team issue
+        // its weights (the nibble box, and at the first stage of each block of 8
+        // groups one box of its scale and bias words), kRecordLanes per team copy the
+        // records of its stages from the call's shared records (all but the first
+        // local_stages, which the team builds itself).  Lane p of a stream issues the
+        // team's stages k with k % lanes = p.  All lanes run one polling loop (no lane
+        // sleeps in a wait that would hold the others back): each tests its next slot
+        // and issues when it is free.
+        constexpr int kWL = kTeams * kWeightLanes;
+        const bool active = lane < kWL + kTeams * kRecordLanes;
+        const bool weights = lane < kWL;
+        const int j = weights ? lane / kWeightLanes : (lane - kWL) / kRecordLanes;
+        const int par = weights ? lane % kWeightLanes : (lane - kWL) % kRecordLanes;
+        const int step = weights ? kWeightLanes : kRecordLanes;
+        const int S = weights ? SN : SR;
+        const int u0 = active ? range_start(p.U, p.R, kTeams * c_id + j) : 0;
+        const int nst = active ? range_start(p.U, p.R, kTeams * c_id + j + 1) - u0 : 0;
+        const int h_loc = p.build ? (nst < H ? nst : H) : 0;     // stages whose records the team builds
+        uint64_t* fullb = weights ? fulln + j * SN : fullr + j * SR;
+        uint64_t* emptyb = weights ? emptyn + j * SN : emptyr + j * SR;
+        int k = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
+        if (!active) k = 0;
+        const uint64_t pol = policy_evict_first();
+        auto issue = [&]() {
+            const int slot = k % S;
+            if (weights) {
+                const int u = u0 + k, t = u / p.GP, gp = u - t * p.GP;
+                const bool sb_new = k == 0 || (u & 3) == 0;
+                mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(kNibStage + (sb_new ? 2 * kSbBox : 0)));
+                tma_load_2d_hint(nib + (j * SN + slot) * kNibStage, &map_nib, &fullb[slot], gp * 64, t * kRowsTile, pol);
+                if (sb_new) {
+                    const int buf = ((u >> 2) - (u0 >> 2)) % kSbBuffers;
+                    tma_load_3d_hint(sb + (j * kSbBuffers + buf) * 2 * kSbBox, &map_sb, &fullb[slot], 8 * (gp >> 2),
+                                     t * kRowsTile, 0, pol);
                 }
-            };
-            // the weight stream needs nothing from the preceding kernel
-            const int pre = nst < kStages ? nst : kStages;
-            for (int si = 0; si < pre; ++si) issue_nibbles(si);
-            int issued = pre, rec_issued = 0;
-            pdl_wait();                                // the x records of this call are complete
-            Q4_TMTR(p, 4002);
-            int gr = gp0;                              // group pair of the next record copy
-            int slot = 0;
-            uint32_t ph = 0;
-            for (int si = 0; si < nst; ++si) {
-                if (si >= kStages) {
-                    if (!wait_or_abort(p, &empty[slot], ph ^ 1u, 1u, abort_flag)) break;
-                    Q4_TMTR(p, si);
-                    issue_nibbles(slot);
-                    ++issued;
-                }
-                uint8_t* dst = smem + slot * kStageBytes + kNibStage;
-                const uint8_t* src = p.xt + (int64_t)(2 * gr) * kRec;
-                if (MT > 8) {
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRec));
-                    bulk_copy_g2s(dst, src, (uint32_t)(2 * kRec), &full[slot]);
-                } else {
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRecHalf));
-                    bulk_copy_g2s(dst, src, (uint32_t)kRecHalf, &full[slot]);
-                    bulk_copy_g2s(dst + kRec, src + kRec, (uint32_t)kRecHalf, &full[slot]);
-                }
-                ++rec_issued;
-                if (++gr == p.GP) gr = 0;
-                if (++slot == kStages) {
-                    slot = 0;
-                    ph ^= 1u;
+            } else {
+                const int gp = (u0 + k) % p.GP;
+                mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(2 * kRec));
+                bulk_copy_g2s(rec + (j * SR + slot) * kRecStage, p.xt + (int64_t)(2 * gp) * kRec, (uint32_t)(2 * kRec),
+                              &fullb[slot]);
+            }
+            k += step;
+        };
+        // the weights' first ring-full needs nothing from the preceding kernel
+        if (active && weights)
+            while (k < nst && k < S) issue();
+        // the records come from this call (or from the preceding glue kernel)
+        pdl_wait();
+        if (lane == 0) Q4_TMGT(p, c_id, 1);
+        bool ok = true;
+        bool records_ok = !p.build;                   // the call's shared records are complete
+        long long idle_since = clock64();
+        while (true) {
+            const bool more = active && ok && k < nst;
+            if (!__any_sync(0xFFFFFFFFu, more)) break;
+            if (more && !weights && !records_ok) {
+                if (ld_acquire_gpu(p.ctl + kCtlBuilt) >= (unsigned)p.G) {
+                    // written through the generic proxy, read by the bulk copies through the async one
+                    fence_proxy_async_global();
+                    records_ok = true;
+                    if (lane == kWL) Q4_TMGT(p, c_id, 2);
                 }
             }
-            // every issued copy must have landed before the CTA may exit; a stage whose
-            // records were never issued (a given-up wait) gets its second arrival without bytes
-            for (int s2 = rec_issued; s2 < issued; ++s2) mbar_arrive(&full[s2 % kStages]);
-            for (int s2 = (issued > kStages ? issued - kStages : 0); s2 < issued; ++s2)
-                mbar_wait(&full[s2 % kStages], (s2 / kStages) & 1, kWaitLimit);
-        }
-    } else if (warp <= kIssuers) {
-        // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
-        const int team = (warp - 1) / kIssuersPerTeam, gsel = (warp - 1) % kIssuersPerTeam;
-        const uint32_t idesc = idesc_bf16_f32(128, W);
-        // B: core matrices K-major, 128 B apart along K, rows 8-15 1024 B after rows 0-7
-        const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(smem + kNibStage + kRecB), 128, 1024);
-        const uint32_t tbase = tmem + (uint32_t)team * kColsTeam;
-        for (int si = team; si < nst; si += kTeams) {
-            const int slot = si % kStages;
-            const int j = si / kTeams;
-            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 2u, abort_flag)))
-                break;
-            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)(j & 1), 2u, abort_flag))) break;
-            tc_fence_after();
-            const uint64_t bd = bdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-            const uint32_t aS = tbase + (a_buffers(W) == 2 ? (uint32_t)(j & 1) * kColsA : 0u);
-            const uint32_t dS = tbase + kColP;
-            if (lane == 0) {
-                if (team == 0 && gsel == 0) Q4_TMTR(p, 2000 + 2 * si);
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    if (g % kIssuersPerTeam != gsel) continue;
-                    const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
-                    // P of group g: W columns (N = W: the record's 8-row blocks, 1024 bytes apart)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ts(dS + (uint32_t)W * g, aS + 32u * g + 8u * kk, bg + 16u * kk, idesc, kk > 0 ? 1u : 0u);
+            bool issued = false;
+            if (more && (weights || records_ok) &&
+                (k < S || mbar_test_wait(&emptyb[k % S], (uint32_t)(((k / S) & 1) ^ 1)))) {
+                issue();
+                issued = true;
+            }
+            if (__any_sync(0xFFFFFFFFu, issued)) {
+                idle_since = clock64();
+            } else {
+                if (*abort_flag) {
+                    ok = false;
+                } else if (clock64() - idle_since > kWaitLimit) {
+                    if (lane == 0) record_timeout(p, kErrProducer, abort_flag);
+                    ok = false;
+                } else {
+                    __nanosleep(64);
                 }
-                tc_commit(&done[team]);
-                if (team == 0 && gsel == 0) Q4_TMTR(p, 2001 + 2 * si);
+            }
+        }
+        if (!ok && active) {
+            // every issued copy must land before the CTA may exit
+            const int first = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
+            for (int k2 = k - step; k2 >= first && k2 + S >= k; k2 -= step) {
+                const int uses = k2 / S - (!weights && k2 % S < h_loc ? 1 : 0);   // earlier copies into that slot
+                mbar_wait(&fullb[k2 % S], (uint32_t)(uses & 1), kWaitLimit);
+            }
+        }
+    } else if (warp <= kTeams) {
+        // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
+        const int team = warp - 1;
+        const int u0 = range_start(p.U, p.R, kTeams * c_id + team);
+        const int nst = range_start(p.U, p.R, kTeams * c_id + team + 1) - u0;
+        // first, this CTA's share of the call's x records (groups c, c + C, ...; this
+        // warp takes every third of them), counted once written
+        if (p.build) {
+            pdl_wait();
+            int nb = 0;
+            for (int g = c_id + team * p.C; g < p.G; g += kTeams * p.C) {
+                build_record_global<W>(p.x, p.M, p.K, g, lane, p.xt);
+                ++nb;
             }
             __syncwarp();
+            if (lane == 0 && nb > 0) {
+                fence_proxy_async_global();
+                red_release_gpu_add(p.ctl + kCtlBuilt, (unsigned)nb);
+            }
+        }
+        const uint32_t idesc = idesc_bf16_f32(128, 16);
+        // B: core matrices K-major, 128 B apart along K, 8-row blocks 1024 B apart
+        const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(rec + team * SR * kRecStage + kRecB), 128, 1024);
+        const uint32_t tbase = tmem + (uint32_t)team * kColsTeam;
+        int rs = 0;
+        for (int k = 0; k < nst; ++k) {
+            // the team hands a stage over only once its records are in shared memory
+            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)(k & 1), kErrIssuer, abort_flag)))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t bd = bdesc0 + (uint64_t)((rs * kRecStage) >> 4);
+                const uint32_t aS = tbase + (a_buffers(W) == 2 ? (uint32_t)(k & 1) * kColsA : 0u);
+                const uint32_t dS = tbase + kColP;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
+                    // P of group g: columns W*g + m (rows 0-15 in one N = 16 MMA, rows 16-31 in another)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                        for (int h = 0; h < W / 16; ++h)
+                            tc_mma_ts(dS + (uint32_t)(W * g + 16 * h), aS + 32u * g + 8u * kk,
+                                      bg + 16u * kk + (uint64_t)(h * (2048 >> 4)), idesc, kk > 0 ? 1u : 0u);
+                    }
+                }
+                tc_commit(&done[team]);
+            }
+            __syncwarp();
+            if (++rs == SR) rs = 0;
         }
         // no MMA of this warp may still run when tensor memory is freed
         if (lane == 0) {
-            tc_commit(&fin[warp - 1]);
-            mbar_wait(&fin[warp - 1], 0, kWaitLimit);
+            tc_commit(&fin[team]);
+            mbar_wait(&fin[team], 0, kWaitLimit);
         }
         __syncwarp();
-    } else if (warp >= kConsumerWarp0) {
+    } else {
         // ------------------------------------------------------------ consumer teams
         const int team = (warp - kConsumerWarp0) >> 2;
         const int q = warp & 3;                        // tensor-memory lane quarter of this warp
-        const int row = q * 32 + lane;                 // row within the tile
-        const uint32_t lane_field = (uint32_t)(q * 32) << 16;
-        const uint32_t tbase = tmem + lane_field + (uint32_t)team * kColsTeam;
+        const int row = q * 32 + lane;                 // row within the tile (and thread within the team)
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)team * kColsTeam;
         const uint32_t dP = tbase + kColP;
-        [[maybe_unused]] const int tr = (lane == 0 && q == 0 && team == 0) ? 1000 : 1 << 20;
+        const int r_id = kTeams * c_id + team;
+        const int u0 = range_start(p.U, p.R, r_id);
+        const int nst = range_start(p.U, p.R, r_id + 1) - u0;
+        const int h_loc = p.build ? (nst < H ? nst : H) : 0;
+        // shared addresses: this team's first nibble slot (its row), first record
+        // slot, first scale/bias buffer (its row's 16 bytes)
+        const uint32_t nib0 = smem_u32(nib) + (uint32_t)(team * SN * kNibStage + row * 64);
+        const uint32_t rec0 = smem_u32(rec) + (uint32_t)(team * SR * kRecStage);
+        const int sx = (row >> 1) & 3;                 // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
+        const uint32_t sb_row = smem_u32(sb) + (uint32_t)(team * kSbBuffers * 2 * kSbBox + row * 16);
 
-        // scale and bias planes: this team's two groups of a stage are one 4-byte word per plane
-        const uint8_t* splane = p.W + p.N * (p.K / 2);
-        const uint8_t* bplane = splane + p.N * p.G * 2;
-        // cursor of the next scale/bias load: the team's stages in order, each
-        // kTeams units after the previous one (no divisions in the loop)
-        int ld_si = team, ld_t = (u0 + team) / p.GP, ld_gp = (u0 + team) - ld_t * p.GP;
-        auto load_next = [&](uint32_t& sv, uint32_t& bv) {
-            const int64_t n = (int64_t)ld_t * kRowsTile + row;
-            if (ld_si < nst && n < p.N) {
-                const int64_t off = (n * p.G + 2 * ld_gp) * 2;
-                sv = __ldg(reinterpret_cast<const uint32_t*>(splane + off));
-                bv = __ldg(reinterpret_cast<const uint32_t*>(bplane + off));
-            } else {
-                sv = 0u;
-                bv = 0u;
-            }
-            ld_si += kTeams;
-            ld_gp += kTeams;
-            while (ld_gp >= p.GP) {
-                ld_gp -= p.GP;
-                ++ld_t;
-            }
-        };
-        // Scale/bias words are loaded two team stages before their constants are
-        // formed, into two register pairs used alternately (the loop below is
-        // unrolled by two), so no instruction reads a register whose load is
-        // still in flight.
-        uint32_t sA, bA, sB, bB;
-        float s0, r0, s1, r1;                          // constants of the stage being dequantized
-        uint32_t cc0, cc1;
-        {
-            uint32_t s_a, b_a;
-            load_next(s_a, b_a);
-            load_next(sA, bA);
-            load_next(sB, bB);
-            group_constants(s_a, b_a, s0, r0, cc0);
-            group_constants(s_a >> 16, b_a >> 16, s1, r1, cc1);
+        // the predecessor may still read y or the scratch, or produce x
+        pdl_wait();
+        if (h_loc > 0) {
+            // the records of the team's first stages, from x, while the call's shared ones are built
+            build_records_smem<W, H>(p.x, p.M, p.K, u0 % p.GP, p.GP, h_loc, row,
+                                     [&](int i) { return rec0 + (uint32_t)(i * kRecStage); });
+            fence_proxy_async_smem();                  // for the MMAs (async proxy)
+            named_barrier(1 + team, 128);              // every row's X before any warp's fold
         }
-        // tile of the team's current stage, advanced the same way
-        int st_t = (u0 + team) / p.GP, st_gp = (u0 + team) - st_t * p.GP;
 
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
         bool live = true;
 
-        // segments: tile t0 + k for k = 0 .. n_seg-1, each closed exactly once by every team
-        const int n_seg = (u1 - 1) / p.GP - t0 + 1;
-        int cur_seg = 0;
-        auto close_segments_before = [&](int seg) {
-            while (cur_seg < seg) {
-                const int tt = t0 + cur_seg;
-                const bool whole = u0 <= tt * p.GP && (tt + 1) * p.GP <= u1;
-                if (team == 0 && row == 0 && cur_seg < 2) Q4_TMGT(p, 2403 + 8 * c_id + 2 * cur_seg);
-                end_segment<MT>(p, acc, red + (red_buffers(W) == 2 ? (cur_seg & 1) : 0) * (kTeams * W * kRowsTile), tt, whole,
-                                cur_seg == 0 ? 0 : 1, team, row, c_id, bcast, !*abort_flag);
-                if (team == 0 && row == 0 && cur_seg < 2) {
-                    Q4_TMGT(p, 2404 + 8 * c_id + 2 * cur_seg);
-#ifdef Q4_TRACE
-                    if (p.trace && !whole && *bcast) p.trace[2407 + 8 * c_id] |= 1ull << cur_seg;
-#endif
-                }
-                ++cur_seg;
-            }
-        };
+        // cursor of the stage being dequantized: ring positions, tile, group pair
+        int ns = 0, rs = 0;
+        uint32_t nph = 0;
+        int st_t = u0 / p.GP, st_gp = u0 - st_t * p.GP;
+        int seg_first_gp = st_gp;                      // group pair at which the current segment started
+        bool first_seg = true;
 
         // the stage handed over in the previous iteration, folded in this one
-        int pend = -1, pend_seg = 0;
+        int pend = -1, pend_t = 0, pend_gp = 0, pend_rs = 0;
+        float s0 = 0.f, r0 = 0.f, s1 = 0.f, r1 = 0.f;  // constants of the stage being dequantized
         float ps0 = 0.f, pr0 = 0.f, ps1 = 0.f, pr1 = 0.f;
-        // hand the team's current stage to its issuer: its A is stored and P is free
+
+#ifdef Q4_TRACE
+        const bool tr = team == 0 && q == 0 && lane == 0 && p.trace;
+        unsigned long long tr_spin = 0, tr_c[6] = {0, 0, 0, 0, 0, 0};
+        long long tr_t = clock64();
+        auto tr_mark = [&](int i) {
+            const long long t = clock64();
+            tr_c[i] += (unsigned long long)(t - tr_t);
+            tr_t = t;
+        };
+        unsigned long long* tr_sp = tr ? &tr_spin : nullptr;
+#else
+        auto tr_mark = [&](int) {};
+        unsigned long long* tr_sp = nullptr;
+#endif
         auto arrive_ready = [&]() {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ready[team]);
         };
-        // signal_ready (W = 16): the hand-over happens as soon as P has been loaded into
-        // registers, so the next MMAs run while this stage's P is folded
+        // fold the pending stage (signal_ready: hand the current stage over as
+        // soon as P is in registers), free its record slot, close its segment if it ends one
         auto fold_pending = [&](bool signal_ready) {
-            const int pslot = pend % kStages;
-            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], (uint32_t)((pend / kTeams) & 1), 4u,
-                                                                 abort_flag));
-            Q4_TMTR(p, tr + 8 * (pend / kTeams) + 7);
-            close_segments_before(pend_seg);
+            tr_mark(5);
+            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &done[team], (uint32_t)(pend & 1), kErrConsumer,
+                                                                 abort_flag, tr_sp));
+            tr_mark(2);
             if (live) {
                 tc_fence_after();
-                const uint8_t* psb = smem + pslot * kStageBytes + kNibStage;
-                const float* xs0 = reinterpret_cast<const float*>(psb);
-                const float* xs1 = reinterpret_cast<const float*>(psb + kRec);
+                const uint32_t xs0 = rec0 + (uint32_t)(pend_rs * kRecStage);
+                const uint32_t xs1 = xs0 + (uint32_t)kRec;
                 if (MT <= 8) {
                     uint32_t P0[8], P1[8];
                     tmem_ld_32x32b_x8(dP, P0);
@@ -693,13 +894,13 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
                     fold_group<MT>(acc, P0, xs0, ps0, pr0);
                     fold_group<MT>(acc, P1, xs1, ps1, pr1);
                 } else if (W == 32) {
-                    // 32 columns per group, one group at a time (registers)
                     uint32_t P[32];
                     tmem_ld_32x32b_x32(dP, P);
                     tmem_wait_ld();
                     fold_group<MT>(acc, P, xs0, ps0, pr0);
                     tmem_ld_32x32b_x32(dP + 32u, P);
                     tmem_wait_ld();
+                    if (signal_ready) arrive_ready();
                     fold_group<MT>(acc, P, xs1, ps1, pr1);
                 } else {
                     uint32_t P0[16], P1[16];
@@ -713,106 +914,118 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const Params p) {
             } else if (signal_ready) {
                 arrive_ready();
             }
-            // that stage's slot (nibbles, records) has been read, and so has P
+            // that stage's records have been read (by the MMAs and the fold), and so has P
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[pslot]);
+            if (lane == 0) mbar_arrive(&emptyr[team * SR + pend_rs]);
+            tr_mark(3);
+            if (pend_gp == p.GP - 1 || pend == nst - 1) {
+                const bool whole = seg_first_gp == 0 && pend_gp == p.GP - 1;
+                end_segment<MT>(p, acc, pend_t, whole, first_seg ? 0 : 1, r_id, q, lane, live && !*abort_flag);
+                if (first_seg && q == 0 && lane == 0) Q4_TMGT(p, c_id, 11 + team);
+                first_seg = false;
+                seg_first_gp = 0;
+            }
         };
 
-        // one team stage: sw/bw hold the words of the team's next stage on entry
-        // and are reloaded with those of the stage after the one that follows
-        auto team_stage = [&](int si, uint32_t& sw, uint32_t& bw) {
-            const int slot = si % kStages;
-            const int j = si / kTeams;
-            Q4_TMTR(p, tr + 8 * j + 0);
-            if (si == 0 && row == 0) Q4_TMGT(p, 2402 + 8 * c_id);
-            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &full[slot], (uint32_t)((si / kStages) & 1), 8u,
-                                                                 abort_flag));
-            Q4_TMTR(p, tr + 8 * j + 1);
+        for (int k = 0; k < nst; ++k) {
+            tr_mark(5);
+            live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &fulln[team * SN + ns], nph, kErrConsumer,
+                                                                 abort_flag, tr_sp));
+            tr_mark(0);
+            if (k == 0 && q == 0 && lane == 0) Q4_TMGT(p, c_id, 3 + team);
+            // scale and bias of this stage's two groups: word st_gp % 4 of the buffer of its block
+            const int sbuf = (((u0 + k) >> 2) - (u0 >> 2)) % kSbBuffers;
+            const uint32_t a = sb_row + (uint32_t)(sbuf * 2 * kSbBox + (st_gp & 3) * 4);
+            const uint32_t sw = lds32(a), bw = lds32(a + kSbBox);
+            uint32_t cc0, cc1;
+            group_constants(sw, bw, s0, r0, cc0);
+            group_constants(sw >> 16, bw >> 16, s1, r1, cc1);
             // one A buffer (W = 32): the previous stage's MMAs must have read it, so fold first
             if (a_buffers(W) == 1 && pend >= 0) fold_pending(false);
-            // dequantize into this stage's A buffer (at W = 16 the other one may still feed the previous MMAs)
+            const uint32_t nb = nib0 + (uint32_t)(ns * kNibStage);
+            const uint4 w0 = lds128(nb + ((0 ^ sx) << 4)), w1 = lds128(nb + ((1 ^ sx) << 4));
+            const uint4 w2 = lds128(nb + ((2 ^ sx) << 4)), w3 = lds128(nb + ((3 ^ sx) << 4));
+            // the nibbles (and this stage's scale/bias words) are in registers: the slot may refill
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&emptyn[team * SN + ns]);
             if (live) {
-                const uint8_t* nb = smem + slot * kStageBytes + row * 64;
-                const int sx = (row >> 1) & 3;         // 64-byte swizzle: chunk index ^ bits 7-8 of the offset
-                const uint32_t aA = tbase + (a_buffers(W) == 2 ? (uint32_t)(j & 1) * kColsA : 0u);
-                uint32_t av0[32], av1[32];
-                {
-                    const uint4 na = *reinterpret_cast<const uint4*>(nb + ((0 ^ sx) << 4));
-                    const uint4 nc = *reinterpret_cast<const uint4*>(nb + ((1 ^ sx) << 4));
-                    dequant64(na, nc, cc0, av0);
-                    tmem_st_32x32b_x32(aA, av0);
-                }
-                {
-                    const uint4 na = *reinterpret_cast<const uint4*>(nb + ((2 ^ sx) << 4));
-                    const uint4 nc = *reinterpret_cast<const uint4*>(nb + ((3 ^ sx) << 4));
-                    dequant64(na, nc, cc1, av1);
-                    tmem_st_32x32b_x32(aA + 32u, av1);
-                }
+                const uint32_t aA = tbase + (a_buffers(W) == 2 ? (uint32_t)(k & 1) * kColsA : 0u);
+                dequant64_store(w0, w1, cc0, aA);
+                dequant64_store(w2, w3, cc1, aA + 32u);
                 tmem_wait_st();
             }
-            Q4_TMTR(p, tr + 8 * j + 2);
-            // fold the previous stage (its MMAs ran meanwhile); then P is free again
-            const bool early = a_buffers(W) == 2 && pend >= 0;   // W = 16: hand over inside the fold
-            if (early) fold_pending(true);
-            Q4_TMTR(p, tr + 8 * j + 3);
-            if (!early) arrive_ready();
-            Q4_TMTR(p, tr + 8 * j + 4);
-            // this stage becomes the pending one; constants of the team's next stage
-            pend = si;
-            pend_seg = st_t - t0;
-            st_gp += kTeams;
-            while (st_gp >= p.GP) {
-                st_gp -= p.GP;
-                ++st_t;
+            tr_mark(1);
+            // the MMAs of this stage read its records, the fold its group sums: a copied
+            // record must have landed before the hand-over (built ones are already there)
+            if (k >= h_loc) {
+                const int uses = k / SR - (rs < h_loc ? 1 : 0);   // earlier copies into this slot
+                live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &fullr[team * SR + rs], (uint32_t)(uses & 1),
+                                                                     kErrConsumer, abort_flag, tr_sp));
             }
+            tr_mark(4);
+            // fold the previous stage (its MMAs ran meanwhile); then P is free again
+            const bool early = a_buffers(W) == 2 && pend >= 0;
+            if (early) fold_pending(true);
+            if (!early) arrive_ready();
+            // this stage becomes the pending one
+            pend = k;
+            pend_t = st_t;
+            pend_gp = st_gp;
+            pend_rs = rs;
             ps0 = s0;
             pr0 = r0;
             ps1 = s1;
             pr1 = r1;
-            group_constants(sw, bw, s0, r0, cc0);
-            group_constants(sw >> 16, bw >> 16, s1, r1, cc1);
-            Q4_TMTR(p, tr + 8 * j + 5);
-            load_next(sw, bw);
-            Q4_TMTR(p, tr + 8 * j + 6);
-        };
-        if (W == 32) {
-            // one stage per iteration (fewer live registers at 32 rows); the prefetched
-            // pairs rotate so that each stage again finds its words in sA, bA
-            for (int si = team; si < nst; si += kTeams) {
-                team_stage(si, sA, bA);
-                const uint32_t ts = sA, tb = bA;
-                sA = sB;
-                bA = bB;
-                sB = ts;
-                bB = tb;
+            if (++st_gp == p.GP) {
+                st_gp = 0;
+                ++st_t;
             }
-        } else {
-            for (int si = team; si < nst; si += 2 * kTeams) {
-                team_stage(si, sA, bA);
-                if (si + kTeams < nst) team_stage(si + kTeams, sB, bB);
+            if (++ns == SN) {
+                ns = 0;
+                nph ^= 1u;
             }
+            if (++rs == SR) rs = 0;
         }
         if (pend >= 0) fold_pending(false);
-        close_segments_before(n_seg);
+        if (q == 0 && lane == 0) Q4_TMGT(p, c_id, 6 + team);
+#ifdef Q4_TRACE
+        if (tr) {
+            p.trace[c_id * 32 + 16] = tr_spin;
+            for (int i = 0; i < 6; ++i) p.trace[c_id * 32 + 18 + i] = tr_c[i];
+            p.trace[c_id * 32 + 24] = (unsigned long long)nst;
+        }
+#endif
     }
 
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        Q4_TMTR(p, 4001);
-        Q4_TMGT(p, 2401 + 8 * c_id);
-    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0) {
+        Q4_TMGT(p, c_id, 9);
+        // the last CTA of the call returns its counters to zero for the next call
+        if (*abort_flag) atomicOr(p.ctl + kCtlAbort, 1u);
+        unsigned old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ctl + kCtlDone) : "memory");
+        if (old == (unsigned)p.C - 1) {
+            if (*reinterpret_cast<volatile unsigned*>(p.ctl + kCtlAbort)) {
+                // a CTA that gave up a wait may have skipped tile arrivals
+                for (int i = 0; i < p.R * 4; ++i) p.sems[i] = 0;
+                p.ctl[kCtlAbort] = 0;
+            }
+            p.ctl[kCtlBuilt] = 0;
+            p.ctl[kCtlDone] = 0;
+        }
     }
 }
 
 template <int MT>
 inline int smem_bytes() { return smem_bytes_w(width<MT>()); }
-inline size_t partial_floats(int C) { return (size_t)C * 2 * 32 * kRowsTile; }   // sized for W = 32
-inline size_t sem_ints(int C) { return (size_t)C; }
+inline size_t partial_floats(int C) { return (size_t)kTeams * C * 2 * 32 * kRowsTile; }   // sized for W = 32
+inline size_t sem_ints(int C) { return (size_t)kTeams * C * 4; }
 
 }  // namespace tm
 }  // namespace q4

@@ -76,14 +76,23 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
  * Row invariance: row m of y is bit-identical for every M (1..32) and every
  * other row's contents.
  * Device memory: the first call on each device (with that device current)
- * allocates the library's scratch -- split-K partial sums, per-tile counters
- * and the prepared x records, about 14 MB on a 152-SM GPU -- and keeps it
- * until the process exits; later calls allocate nothing.  Make that first
- * call outside any stream capture.  Every call on a device shares this
- * scratch, so calls that may run at the same time on one device (different
- * streams without an ordering between them) race and give wrong results:
- * order them on one stream or with events.
- * Accuracy: |y - exact| <= 2e-3 * sum_k |x[m,k] w[n,k]| per output. */
+ * allocates the library's scratch -- split-K partial sums, per-tile and
+ * per-call counters and the call's x records, about 25 MB on a 152-SM GPU --
+ * and keeps it until the process exits; later calls allocate nothing.  Make
+ * that first call outside any stream capture.  Every call on a device shares
+ * this scratch, so calls that may run at the same time on one device (different
+ * streams without an ordering between them) race and give wrong results: order
+ * them on one stream or with events.
+ * Residency: the kernel runs one CTA per SM and its CTAs exchange the call's x
+ * records, so all of them must be resident at once.  A context that gets fewer
+ * SMs than the device reports (an MPS client limited to a share of the SMs, for
+ * example) can leave a CTA waiting for one that never starts; the wait gives up
+ * after about a second and q4_device_status() reports Q4_ERR_TIMEOUT.
+ * Accuracy: |y - exact| <= 2e-3 * sum_k |x[m,k] w[n,k]| per output, for
+ * activations with |x| < 2^28 whose nonzero values are at least 2^-93 in
+ * magnitude, and scales with |s| < 2^95 (the tensor core sees x scaled by
+ * 2^100 or 2^96 and products scaled by 2^-33: outside that range they overflow
+ * or fall below the fp32 normal range). */
 q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     q4_stream_t stream);
 
@@ -93,16 +102,18 @@ q4_status q4_matmul(const void* x, const void* W, int M, int64_t N, int64_t K, f
  * that runs inside a host application owning the device allocator, or a
  * latency-critical loop that cannot afford cudaMalloc's implicit device
  * synchronisation.
- *   Arguments, layout, result and accuracy are those of q4_matmul, except
- *   that M is limited to 1..16; the caller still owns x, W and y.  K is
- *   limited to 20480 and the device to
- *   160 SMs (larger: Q4_ERR_UNSUPPORTED_SHAPE / Q4_ERR_UNSUPPORTED_DEVICE,
- *   nothing launched).
- *   Scratch: a fixed array inside the library's device image (about 8.2 MB),
- *   which every device that loads the library holds until the process exits.
- *   No call allocates or frees device memory.  The first call on a device,
- *   with that device current, looks up the array's device address and sets
- *   kernel attributes; make that first call before any stream capture.
+ *   Arguments, layout and the accuracy bound are those of q4_matmul, except
+ *   that M is limited to 1..16; the caller still owns x, W and y.  Rows are
+ *   bit-identical for every M and across runs, as with q4_matmul, but this call
+ *   runs a different kernel, so its bits may differ from q4_matmul's.  K is
+ *   limited to 20480 and the device to 160 SMs (larger:
+ *   Q4_ERR_UNSUPPORTED_SHAPE / Q4_ERR_UNSUPPORTED_DEVICE, nothing launched).
+ *   Scratch: a fixed array of 8,542,208 bytes inside the library's device
+ *   image, which every device that loads the library holds until the process
+ *   exits.  No call allocates or frees device memory, and neither does
+ *   q4_device_status().  The first call on a device, with that device current,
+ *   looks up the array's device address and sets kernel attributes; make that
+ *   first call before any stream capture.
  *   Every call clears the counters it needs at zero (an asynchronous memset
  *   on `stream`) and overwrites the rest before reading it.
  *   All calls on one device share the one array, so calls that may run at the
@@ -240,8 +251,10 @@ q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream);
 /* Synchronizes `stream` and reports whether any kernel of this library on the
  * current device recorded a device-side failure since the last query -- an
  * out-of-range codebook id (Q4_ERR_INVALID_INDEX, reported first) or a bounded
- * wait that gave up (Q4_ERR_TIMEOUT) -- then clears that record.  Q4_OK
- * otherwise. */
+ * wait that gave up (Q4_ERR_TIMEOUT) -- then clears that record.  After a wait
+ * that gave up it also returns the library's arrival counters to zero (a CTA
+ * that gave up may have skipped its arrivals), so later calls start clean.
+ * Allocates no device memory.  Q4_OK otherwise. */
 q4_status q4_device_status(q4_stream_t stream);
 
 /* Thread-local description of the last failure on this thread ("" if none). */

@@ -143,3 +143,31 @@ def test_wide_dynamic_range():
     W = P.hand_pack(q, s, b)
     x = torch.from_numpy(xr).to(torch.bfloat16)
     run_and_check(x, torch.from_numpy(W), N, K, what="dynamic range")
+
+
+def _bf16_magnitudes(rng, shape, lo_exp, hi_exp):
+    """Random signs, |x| uniform in binades [2^lo_exp, 2^hi_exp), as bf16-exact float32."""
+    e = rng.integers(lo_exp, hi_exp, size=shape)
+    v = rng.choice([-1.0, 1.0], size=shape) * (1.0 + rng.random(shape)) * np.exp2(e)
+    return (v.astype(np.float32).view(np.uint32) & 0xFFFF0000).view(np.float32)
+
+
+def test_x_range_window_edges():
+    """The activation range the header states, |x| in [2^-93, 2^28): rows drawn
+    from the lowest binades (2^-93 .. 2^-90), from the highest (2^26 .. 2^27),
+    and rows mixing both ends with normal values, against the oracle."""
+    rng = np.random.default_rng(23)
+    N, K, M = 200, 2048, 16
+    W = si.make_weights(N, K, 29)
+    xr = rng.standard_normal((M, K)).astype(np.float32)
+    xr = (xr.view(np.uint32) & 0xFFFF0000).view(np.float32)
+    xr[0] = _bf16_magnitudes(rng, K, -93, -90)
+    xr[3] = _bf16_magnitudes(rng, K, 27, 28)                  # the top binade: |x| < 2^28
+    xr[7] = _bf16_magnitudes(rng, K, -93, 27)                 # every binade of the window in one row
+    xr[9, : K // 2] = _bf16_magnitudes(rng, K // 2, -93, -92)
+    xr[9, K // 2:] = _bf16_magnitudes(rng, K // 2, 27, 28)
+    xr[15] = 0.0
+    xr[15, ::97] = _bf16_magnitudes(rng, xr[15, ::97].shape, -93, -92)   # a sparse row of tiny values
+    x = torch.from_numpy(xr).to(torch.bfloat16)
+    for rows in (slice(0, 16), slice(0, 1), slice(3, 4), slice(15, 16)):
+        run_and_check(x[rows].contiguous(), W, N, K, what=f"x range rows {rows}")

@@ -23,7 +23,7 @@ def _y(x, W, N, K):
     return q4.matmul(x.contiguous(), W, N, K).cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "attn_in", "down", "gdn_out"])
+@pytest.mark.parametrize("name", ["tiny", "attn_in", "gate_up", "down", "gdn_in", "gdn_out", "lm_head"])
 def test_rows_identical_across_M(name):
     N, K = si.SHAPES[name]
     W = si.make_weights(N, K, 5, device="cuda")
