@@ -339,6 +339,8 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
     p.U = p.T * p.GP;
     p.C = grid_ctas(p.U, d.sm_count);
     p.R = kTeams * p.C;
+    p.q_units = p.U / p.R;
+    p.rem_units = p.U % p.R;
     p.build = records_ready ? 0 : 1;   // else the preceding glue kernel wrote the records
 #ifdef Q4_TRACE
     p.trace = g_trace;

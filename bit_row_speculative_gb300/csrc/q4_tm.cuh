@@ -176,6 +176,8 @@ struct Params {
     int U;                      // T * GP units
     int C;                      // CTAs (grid size)
     int R;                      // 3 * C ranges
+    int q_units;                // U / R: every range has q_units units, the first rem_units one more
+    int rem_units;              // U % R
     int build;                  // 1: build the x records here; 0: the preceding glue kernel wrote them
 #ifdef Q4_TRACE
     unsigned long long* trace;  // developer timing trace (compiled in only with Q4_TRACE)
@@ -205,15 +207,14 @@ inline int grid_ctas(int U, int sm_count) {
     return c < sm_count ? c : sm_count;
 }
 
-// First unit of range r.
-__host__ __device__ __forceinline__ int range_start(int U, int R, int r) { return (int)(((int64_t)U * r) / R); }
+// Ranges: the first rem ranges have q + 1 units, the others q (q = U / R, rem =
+// U % R), so range r starts at r*q + min(r, rem) -- 32-bit arithmetic only.
+__host__ __device__ __forceinline__ int range_start(int q, int rem, int r) { return r * q + (r < rem ? r : rem); }
 
-// The (non-empty) range that owns unit u: the largest r with range_start(r) <= u.
-__device__ __forceinline__ int range_of_unit(int U, int R, int u) {
-    int r = (int)(((int64_t)u * R) / U);
-    while (r + 1 < R && range_start(U, R, r + 1) <= u) ++r;
-    while (r > 0 && range_start(U, R, r) > u) --r;
-    return r;
+// The range that owns unit u (0 <= u < U).
+__device__ __forceinline__ int range_of_unit(int q, int rem, int u) {
+    const int big = (q + 1) * rem;                  // units in the longer ranges
+    return u < big ? u / (q + 1) : rem + (q > 0 ? (u - big) / q : 0);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -510,7 +511,7 @@ __device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, 
 // y.  Kept out of line (rare); it takes no reference to the caller's sums.
 template <int MT>
 __device__ __noinline__ void finish_tile(const float* __restrict__ partials, float* __restrict__ y, int64_t N, int M,
-                                         int U, int R, int GP, int t, int row, int r_first, int r_last) {
+                                         int q, int rem, int GP, int t, int row, int r_first, int r_last) {
     constexpr int W = width<MT>();
     const int64_t n = (int64_t)t * kRowsTile + row;
     float v[MT];
@@ -523,9 +524,8 @@ __device__ __noinline__ void finish_tile(const float* __restrict__ partials, flo
 #pragma unroll
         for (int i = 0; i < kB; ++i) {
             const int rr = rb + i;
-            const int rs = range_start(U, R, rr);
-            const bool use = rr <= r_last && rs < range_start(U, R, rr + 1);
-            const int cslot = (rs / GP == t) ? 0 : 1;   // the tile is rr's first segment, or its last
+            const bool use = rr <= r_last;
+            const int cslot = range_start(q, rem, rr) >= t * GP ? 0 : 1;   // the tile is rr's first segment, or its last
             const float* src = partials + (((int64_t)rr * 2 + cslot) * W) * kRowsTile + row;
 #pragma unroll
             for (int m = 0; m < MT; ++m) pv[i][m] = use ? __ldcg(src + m * kRowsTile) : 0.0f;
@@ -571,11 +571,9 @@ __device__ __forceinline__ void end_segment(const Params& p, float (&acc)[MT], i
         // every lane's reads in finish_tile
         __syncwarp();
         const int tu = t * p.GP;
-        const int r_first = range_of_unit(p.U, p.R, tu);
-        const int r_last = range_of_unit(p.U, p.R, tu + p.GP - 1);
-        int count = 0;                                 // non-empty ranges contributing to tile t
-        for (int rr = r_first; rr <= r_last; ++rr)
-            count += range_start(p.U, p.R, rr) < range_start(p.U, p.R, rr + 1) ? 1 : 0;
+        const int r_first = range_of_unit(p.q_units, p.rem_units, tu);
+        const int r_last = range_of_unit(p.q_units, p.rem_units, tu + p.GP - 1);
+        const int count = r_last - r_first + 1;        // ranges contributing to tile t (none of them empty)
         int last = 0;
         if (lane == 0) {
             int* sem = p.sems + r_first * 4 + q;
@@ -588,7 +586,7 @@ __device__ __forceinline__ void end_segment(const Params& p, float (&acc)[MT], i
         }
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
         __syncwarp();
-        if (last) finish_tile<MT>(p.partials, p.y, p.N, p.M, p.U, p.R, p.GP, t, row, r_first, r_last);
+        if (last) finish_tile<MT>(p.partials, p.y, p.N, p.M, p.q_units, p.rem_units, p.GP, t, row, r_first, r_last);
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
@@ -678,8 +676,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const int par = weights ? lane % kWeightLanes : (lane - kWL) % kRecordLanes;
         const int step = weights ? kWeightLanes : kRecordLanes;
         const int S = weights ? SN : SR;
-        const int u0 = active ? range_start(p.U, p.R, kTeams * c_id + j) : 0;
-        const int nst = active ? range_start(p.U, p.R, kTeams * c_id + j + 1) - u0 : 0;
+        const int u0 = active ? range_start(p.q_units, p.rem_units, kTeams * c_id + j) : 0;
+        const int nst = active ? range_start(p.q_units, p.rem_units, kTeams * c_id + j + 1) - u0 : 0;
         const int h_loc = p.build ? (nst < H ? nst : H) : 0;     // stages whose records the team builds
         uint64_t* fullb = weights ? fulln + j * SN : fullr + j * SR;
         uint64_t* emptyb = weights ? emptyn + j * SN : emptyr + j * SR;
@@ -756,8 +754,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     } else if (warp <= kTeams) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
         const int team = warp - 1;
-        const int u0 = range_start(p.U, p.R, kTeams * c_id + team);
-        const int nst = range_start(p.U, p.R, kTeams * c_id + team + 1) - u0;
+        const int u0 = range_start(p.q_units, p.rem_units, kTeams * c_id + team);
+        const int nst = range_start(p.q_units, p.rem_units, kTeams * c_id + team + 1) - u0;
         // first, this CTA's share of the call's x records (groups c, c + C, ...; this
         // warp takes every third of them), counted once written
         if (p.build) {
@@ -818,8 +816,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)team * kColsTeam;
         const uint32_t dP = tbase + kColP;
         const int r_id = kTeams * c_id + team;
-        const int u0 = range_start(p.U, p.R, r_id);
-        const int nst = range_start(p.U, p.R, r_id + 1) - u0;
+        const int u0 = range_start(p.q_units, p.rem_units, r_id);
+        const int nst = range_start(p.q_units, p.rem_units, r_id + 1) - u0;
         const int h_loc = p.build ? (nst < H ? nst : H) : 0;
         // shared addresses: this team's first nibble slot (its row), first record
         // slot, first scale/bias buffer (its row's 16 bytes)
