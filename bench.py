@@ -50,7 +50,10 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["attn_sweep", "attn_wide", "lm_head", "mlp_gdn", "full_pass", "draft_edges"], default="attn_sweep")
-    p.add_argument("--reps", type=int, default=20, help="calls per M per step")
+    p.add_argument("--reps", type=int, default=20, help="calls per graph (one graph per M)")
+    p.add_argument("--graph-replays", type=int, default=50, help="replays of each M's graph per step")
+    p.add_argument("--no-configs", action="store_true", help="attention sweep only (skip the other 27B shapes, "
+                   "the LM head and the full pass)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -260,11 +263,34 @@ def timed_region(run, gpu_id, world, dev, sync, status, sampler_cls=None, settle
 _CPU_INPUTS = {}
 
 
-def cpu_oracle_sample(spec, seconds, seed=0):
+def cpu_model():
+    """The host CPU's model name from /proc/cpuinfo (on Arm, implementer and part
+    numbers when no name is given), and the machine type."""
+    import platform
+    name, impl, part = None, None, None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                k, _, v = line.partition(":")
+                k, v = k.strip().lower(), v.strip()
+                if k in ("model name", "cpu model") and not name:
+                    name = v
+                elif k == "cpu implementer" and not impl:
+                    impl = v
+                elif k == "cpu part" and not part:
+                    part = v
+    except OSError:
+        pass
+    if not name and impl:
+        name = f"Arm CPU implementer {impl} part {part}" + (" (Neoverse V2, as in Grace)" if (impl, part) == ("0x41", "0xd4f") else "")
+    return f"{name or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical CPUs)"
+
+
+def cpu_oracle_sample(spec, seconds, seed=0, single_core=False):
     """Time the CPU oracle on a bounded sample of the workload: every M of the
     sweep over a run of output columns (the whole matrix, repeated, when the
     host is fast enough), about `seconds` of wall time; GB/s with the same byte
-    formula as the GPU line."""
+    formula as the GPU line.  single_core: also the same on one thread."""
     import numpy as np
     import oracle
     import synth_inputs as si
@@ -275,25 +301,33 @@ def cpu_oracle_sample(spec, seconds, seed=0):
         _CPU_INPUTS[key] = (si.make_weights(N, K, 424242).numpy(),
                             {M: si.bf16_bits(si.make_x(M, K, 99 + M)).numpy().view(np.uint16) for M in set(Ms)})
     W, xs = _CPU_INPUTS[key]
-    threads = os.cpu_count() or 1
-    # calibrate on a probe of 16 columns per thread
-    probe = min(N, 16 * threads)
-    t0 = time.perf_counter()
-    for M in Ms:
-        oracle.matmul(xs[M], W, N, K, cols=np.arange(probe), threads=threads)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    want = max(probe, int(probe * seconds / dt))
-    ncols, reps = (want, 1) if want <= N else (N, max(1, round(want / N)))
-    cols = np.arange(ncols)
-    t0 = time.perf_counter()
-    for _ in range(reps):
+
+    def timed(threads, secs):
+        # calibrate on a probe of 16 columns per thread
+        probe = min(N, 16 * threads)
+        t0 = time.perf_counter()
         for M in Ms:
-            oracle.matmul(xs[M], W, N, K, cols=cols, threads=threads)
-    el = time.perf_counter() - t0
-    nbytes = reps * sum(call_bytes(M, ncols, K) for M in Ms)
-    what = f"first {ncols} of {N} output columns" if reps == 1 else f"all {N} output columns, {reps} times"
-    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{label} K={K}, {what}, M in {Ms}, fp64 oracle on {threads} threads, {el:.1f} s wall"}
+            oracle.matmul(xs[M], W, N, K, cols=np.arange(probe), threads=threads)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        want = max(probe, int(probe * secs / dt))
+        ncols, reps = (want, 1) if want <= N else (N, max(1, round(want / N)))
+        cols = np.arange(ncols)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            for M in Ms:
+                oracle.matmul(xs[M], W, N, K, cols=cols, threads=threads)
+        el = time.perf_counter() - t0
+        nbytes = reps * sum(call_bytes(M, ncols, K) for M in Ms)
+        what = f"first {ncols} of {N} output columns" if reps == 1 else f"all {N} output columns, {reps} times"
+        return nbytes / el / 1e9, f"{label} K={K}, {what}, M in {Ms}, fp64 oracle on {threads} thread(s), {el:.1f} s wall"
+
+    threads = os.cpu_count() or 1
+    value, sample = timed(threads, seconds)
+    out = {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample, "cpu": cpu_model()}
+    if single_core:
+        v1, s1 = timed(1, max(1.0, seconds / 3))
+        out["single_core"] = {"value": v1, "unit": "GB/s", "cores": 1, "sample": s1}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -460,7 +494,8 @@ def run_ours(args, rank, world, local_rank):
 
     # prediction first: the byte count and the ceiling at the measured peak
     peak, peak_kind = read_peaks()
-    step_bytes = sum(call_bytes(M, N, K) for _, N, K, Ms in spec for M in Ms) * args.reps
+    replays = max(1, args.graph_replays)
+    step_bytes = sum(call_bytes(M, N, K) for _, N, K, Ms in spec for M in Ms) * args.reps * replays
     if rank == 0:
         print(f"prediction: {step_bytes / 1e9:.3f} GB per step at {peak:.0f} GB/s ({peak_kind}) "
               f"-> {step_bytes / peak / 1e6:.3f} ms per step floor", file=sys.stderr, flush=True)
@@ -524,7 +559,8 @@ def run_ours(args, rank, world, local_rank):
             for _ in range(args.steps):
                 for i, (label, N, K, M, g) in enumerate(graphs):
                     evs[i][0].record(stream)
-                    g.replay()
+                    for _ in range(replays):
+                        g.replay()
                     evs[i][1].record(stream)
                 # accumulate per-graph times after each step (events are reused)
                 stream.synchronize()
@@ -543,7 +579,7 @@ def run_ours(args, rank, world, local_rank):
 
     per_m = {}
     for i, (label, N, K, M, g) in enumerate(graphs):
-        us = per_graph_ms[i] / (args.steps * args.reps) * 1e3
+        us = per_graph_ms[i] / (args.steps * args.reps * replays) * 1e3
         per_m[f"{label}_M{M}"] = {"us_per_call": round(us, 3),
                                   "GBs": round(call_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
     ratio = ratio32 = None
@@ -600,11 +636,11 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through the public API with host buffers: per call, pinned
     # host x -> device, the matmul, device y -> pinned host
-    e2e = e2e_pipelined(args, spec, pools, xs, ys, stream, dev, world, step_bytes)
+    e2e = e2e_pipelined(args, spec, pools, xs, ys, stream, dev, world, step_bytes // replays)
 
     if rank != 0:
         return
-    n_calls = sum(len(Ms) for _, _, _, Ms in spec) * args.reps
+    n_calls = sum(len(Ms) for _, _, _, Ms in spec) * args.reps * replays
     achieved = step_bytes / (kernel_ms / args.steps / 1e3) / 1e9
     traffic = read_traffic(args.workload)
     line = {
@@ -612,10 +648,11 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(kernel_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x, q4 weights, fp32 accumulate",
         "data": "synthetic (seeded; nibbles uniform 0..15, scale |N(0,1)|*0.01, bias -8*scale+N(0,1e-3), x N(0,1))",
-        "config": {"workload": desc, "calls_per_M_per_step": args.reps,
+        "config": {"workload": desc, "calls_per_M_per_step": args.reps * replays,
                    "l2": f"rotating pool of {len(next(iter(pools.values())))} weight copies "
                          f"({sum(w.numel() for w in next(iter(pools.values()))) / 1e6:.0f} MB) > L2 "
-                         f"({l2 / 2**20:.0f} MiB); one CUDA graph per M",
+                         f"({l2 / 2**20:.0f} MiB); one CUDA graph of {args.reps} calls per M, replayed {replays} "
+                         f"times per step",
                    "parallelism": f"replicas x{world}"},
         "per_M": per_m, "ratio_M16_over_M1": None if ratio is None else round(ratio, 4),
         "ratio_M32_over_M1": None if ratio32 is None else round(ratio32, 4),
@@ -627,12 +664,149 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": n_calls * launches_per_call * args.steps,
         "clocks": clocks, "e2e": e2e, "timed_region_ms": round(total_ms, 3),
     }
+    if args.workload == "attn_sweep" and not args.no_configs:
+        del pools, graphs
+        torch.cuda.empty_cache()
+        line["per_shape"] = model_shapes(args, world, dev, l2, peak, peak_kind, stream)
     if not args.no_cpu_baseline:
         try:
-            line["cpu_baseline"] = cpu_oracle_sample(spec, args.cpu_seconds)
+            line["cpu_baseline"] = cpu_oracle_sample(spec, args.cpu_seconds, single_core=True)
         except Exception as exc:                     # report, do not hide
             line["cpu_baseline"] = {"error": repr(exc)}
     print(json.dumps(check_roofline(line)), flush=True)
+
+
+def time_calls(enqueue, n_calls, replays, stream, world, dev):
+    """Device microseconds per call of `enqueue(i)` (i = 0 .. n_calls-1), captured
+    once in a CUDA graph and replayed `replays` times; the max over ranks."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(min(n_calls, 6)):
+            enqueue(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            enqueue(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1) / (replays * n_calls) * 1e3, world, dev)
+
+
+def model_shapes(args, world, dev, l2, peak, peak_kind, stream):
+    """The other shapes of the 27B-class model at full size, each timed on its own
+    (the MLP and GDN projections at M = 1 and 16, the LM head at M = 16), then the
+    full chained pass at M = 16 with its time split by layer type (the same
+    kernels run layer by layer, with events around each launch)."""
+    import torch
+    import bit_row_speculative_gb300 as q4
+    import synth_inputs as si
+    out = {}
+
+    def entry(us, M, N, K, what):
+        gbs = call_bytes(M, N, K) / (us * 1e-6) / 1e9
+        return {"us_per_call": round(us, 3), "GBs": round(gbs, 1), "frac": round(gbs / peak, 4), "what": what}
+
+    # config 3: gate/up, down, GDN in, GDN out; M = 1 and 16; rotating pools > 4x L2
+    for name in ("gate_up", "down", "gdn_in", "gdn_out"):
+        N, K = si.SHAPES[name]
+        copies = max(2, -(-4 * l2 // (N * K * 9 // 16)))
+        base = si.make_weights(N, K, si.w_seed(3, list(si.SHAPES).index(name)), device=dev)
+        pool = [base] + [base.clone() for _ in range(copies - 1)]
+        for M in (1, 16):
+            x = si.make_x(M, K, si.x_seed(3) + M, device=dev)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            us = time_calls(lambda i: q4.matmul(x, pool[i % copies], N, K, y=y, stream=stream), 20, 10, stream,
+                            world, dev)
+            out[f"{name}_M{M}"] = entry(us, M, N, K, f"K={K}->N={N}, {copies} weight copies rotating")
+        del pool, base
+    # config 4: the LM head, twice per step (target verify and draft readout, different x)
+    N, K = si.SHAPES["lm_head"]
+    heads = [si.make_weights(N, K, si.w_seed(4, t), device=dev) for t in range(2)]
+    xh = [si.make_x(16, K, si.x_seed(4) + t, device=dev) for t in range(2)]
+    yh = torch.empty((16, N), dtype=torch.float32, device=dev)
+    us = time_calls(lambda i: q4.matmul(xh[i % 2], heads[i % 2], N, K, y=yh, stream=stream), 10, 5, stream, world, dev)
+    out["lm_head_M16"] = entry(us, 16, N, K, f"K={K}->N={N}, two heads alternating")
+    del heads, xh, yh
+    torch.cuda.empty_cache()
+    # config 5: the full pass, one q4_decode_step; then the same launches layer by layer
+    spec = si.full_pass_spec()
+    M = 16
+    layers = [(si.make_weights(Nn, Kk, si.w_seed(5, t), device=dev), Nn, Kk, g) for t, (Nn, Kk, g) in enumerate(spec)]
+    x0 = si.make_x(M, spec[0][1], si.x_seed(5), device=dev)
+    y = torch.empty((M, spec[-1][0]), dtype=torch.float32, device=dev)
+    ws = torch.empty(q4.decode_step_workspace_bytes(layers, M), dtype=torch.uint8, device=dev)
+    step_ms = time_calls(lambda i: q4.decode_step(layers, x0, y_last=y, workspace=ws, stream=stream), 1, 5, stream,
+                         world, dev) / 1e3
+    step_bytes = sum(call_bytes(M, Nn, Kk) for Nn, Kk, _ in spec)
+    types = {}
+    ybuf = torch.empty(M * max(Nn for Nn, _, _ in spec), dtype=torch.float32, device=dev)
+    xbuf = torch.empty(M * max(Kk for _, Kk, _ in spec), dtype=torch.bfloat16, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * len(spec))]
+
+    def kind(t, Nn, Kk):
+        i = t // 4
+        if t >= 4 * 64:
+            return "lm_head"
+        return ["attn_in" if i % 4 == 3 else "gdn_in", "attn_out" if i % 4 == 3 else "gdn_out", "gate_up",
+                "down"][t % 4]
+
+    for rep in range(3):
+        with torch.cuda.stream(stream):
+            xj = x0
+            for t, (W, Nn, Kk, g) in enumerate(layers):
+                yj = y if t + 1 == len(layers) else ybuf[:M * Nn].view(M, Nn)
+                evs[2 * t][0].record(stream)
+                q4.matmul(xj, W, Nn, Kk, y=yj, stream=stream)
+                evs[2 * t][1].record(stream)
+                if t + 1 < len(layers):
+                    Kn = layers[t + 1][2]
+                    xn = xbuf[:M * Kn].view(M, Kn)
+                    evs[2 * t + 1][0].record(stream)
+                    q4.glue(yj, Kn, g, x_next=xn, stream=stream)
+                    evs[2 * t + 1][1].record(stream)
+                    xj = xn
+        stream.synchronize()
+        if rep < 2:
+            continue
+        for t, (W, Nn, Kk, g) in enumerate(layers):
+            k = kind(t, Nn, Kk)
+            d = types.setdefault(k, {"layers": 0, "ms": 0.0, "bytes": 0})
+            d["layers"] += 1
+            d["ms"] += evs[2 * t][0].elapsed_time(evs[2 * t][1])
+            d["bytes"] += call_bytes(M, Nn, Kk)
+            if t + 1 < len(layers):
+                gd = types.setdefault("glue", {"layers": 0, "ms": 0.0, "bytes": 0})
+                gd["layers"] += 1
+                gd["ms"] += evs[2 * t + 1][0].elapsed_time(evs[2 * t + 1][1])
+                gd["bytes"] += M * Nn * 4 + M * layers[t + 1][2] * 2
+    total = sum(d["ms"] for d in types.values())
+    split = {}
+    for k, d in types.items():
+        gbs = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+        split[k] = {"layers": d["layers"], "ms": round(d["ms"], 4), "share": round(d["ms"] / total, 4),
+                    "GBs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    gbs = step_bytes / (step_ms * 1e-3) / 1e9
+    out["full_pass_M16"] = {"ms_per_step": round(step_ms, 4), "GBs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                            "what": f"{len(spec)} linears + glue in one q4_decode_step (CUDA graph), "
+                                    f"{sum(Nn * Kk * 9 // 16 for Nn, Kk, _ in spec) / 1e9:.3f} GB of weights",
+                            "by_layer_type": split,
+                            "by_layer_type_how": "the same layers run as separate q4_matmul / q4_glue calls with "
+                                                 "events around each launch (eager), "
+                                                 f"{total:.3f} ms in all"}
+    del layers
+    torch.cuda.empty_cache()
+    out["peak"] = {"GBs": peak, "kind": peak_kind}
+    return out
 
 
 def run_full_pass(args, rank, world, local_rank):
