@@ -193,6 +193,7 @@ cudaError_t reset_counters(int dev) {
     DeviceInfo& d = g_devices[dev];
     if (!d.ready || d.status != Q4_OK) return cudaSuccess;
     cudaError_t e = cudaMemset(d.sems, 0, d.sem_bytes);
+    if (e == cudaSuccess) e = cudaMemset(d.ctl, 0, q4::tm::kCtlWords * sizeof(unsigned int));
     if (e == cudaSuccess) e = cudaMemset(d.topk_tickets, 0, (size_t)Q4_MAX_ROWS * sizeof(int));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     return e;
@@ -299,6 +300,34 @@ q4_status launch_tc(const DeviceInfo& d, const void* x, const void* W, int M, in
     return Q4_OK;
 }
 
+// Work split of the tensor-memory kernel, from T, GP and the SM count only.
+// Stream-K over all tiles by default: R = 3C ranges of about U / R units, which
+// cross tile boundaries, so most ranges end two partial tiles.  Where the tiles
+// divide among the teams (S = floor(3C / T) >= 2 ranges per tile, no longer than
+// the stream-K ranges), every range lies inside one tile instead and ends just
+// one partial tile: the attention and out-projection shapes.
+void plan_ranges(q4::tm::Params& p, int sm_count) {
+    using namespace q4::tm;
+    const int C0 = grid_ctas(p.U, sm_count);
+    const int R0 = kTeams * C0;
+    const int q_stream = (p.U + R0 - 1) / R0;         // longest stream-K range
+    int s = R0 / p.T;
+    if (s > p.GP) s = p.GP;
+    if (s >= 2 && (p.GP + s - 1) / s <= q_stream) {
+        p.S = s;
+        p.L = p.GP;
+        p.R = p.T * s;
+        p.C = (p.R + kTeams - 1) / kTeams;
+    } else {
+        p.S = R0;
+        p.L = p.U;
+        p.R = R0;
+        p.C = C0;
+    }
+    p.q_units = p.L / p.S;
+    p.rem_units = p.L % p.S;
+}
+
 q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, int64_t N, int64_t K, float* y,
                     cudaStream_t stream, bool records_ready) {
     using namespace q4::tm;
@@ -337,10 +366,7 @@ q4_status launch_tm(const DeviceInfo& d, const void* x, const void* W, int M, in
     p.GP = p.G / 2;
     p.T = (int)((N + kRowsTile - 1) / kRowsTile);
     p.U = p.T * p.GP;
-    p.C = grid_ctas(p.U, d.sm_count);
-    p.R = kTeams * p.C;
-    p.q_units = p.U / p.R;
-    p.rem_units = p.U % p.R;
+    plan_ranges(p, d.sm_count);
     p.build = records_ready ? 0 : 1;   // else the preceding glue kernel wrote the records
 #ifdef Q4_TRACE
     p.trace = g_trace;

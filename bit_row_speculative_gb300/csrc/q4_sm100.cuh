@@ -178,6 +178,32 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 }
 
 // D[tmem] (+)= A[tmem] x B[smem]^T, kind::f16 (bf16 operands, fp32 accumulate).
+// 1 in one lane of a converged warp (the lowest active one), 0 in the others.
+__device__ __forceinline__ uint32_t elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e;
+}
+// tcgen05.mma with A in tensor memory and tcgen05.commit, issued only by the lane
+// where `leader` is nonzero.  The whole warp executes them converged, with
+// warp-uniform operands, so the operand arithmetic stays warp-uniform.
+__device__ __forceinline__ void tc_mma_ts_if(uint32_t leader, uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred pl, pa;\n\t"
+        "setp.ne.b32 pl, %5, 0;\n\t"
+        "setp.ne.b32 pa, %4, 0;\n\t"
+        "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t}" ::"r"(d_taddr),
+        "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_if(uint32_t leader, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred pl;\n\tsetp.ne.b32 pl, %1, 0;\n\t"
+        "@pl tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(leader)
+        : "memory");
+}
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(

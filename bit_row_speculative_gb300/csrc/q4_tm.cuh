@@ -69,11 +69,13 @@
 // nothing in the arithmetic of row m depends on the other rows, so every row's
 // result is independent of M and of the run.
 // Every barrier wait is bounded; a wait that runs out sets the error word and
-// the CTA runs to its end without further waiting.  The last CTA to finish
-// returns the call's counters to zero (and the tile counters too after a
-// timed-out wait), so the next call starts clean.  All CTAs of a call must be
-// resident together (one per SM, as launched): a CTA waits for the records the
-// others build.
+// the CTA runs to its end without further waiting.  Counters return to zero
+// within the call: a tile quarter's counter by its last contributor, the record
+// counters by the last CTA whose record readers have all seen the records (so
+// no CTA ends with a round trip to memory).  A call that gave up a wait may
+// leave them set; the status query that reports the timeout clears them.  All
+// CTAs of a call must be resident together (one per SM, as launched): a CTA
+// waits for the records the others build.
 #pragma once
 
 #include <cuda.h>
@@ -154,8 +156,7 @@ constexpr unsigned kErrProducer = 1u, kErrIssuer = 2u, kErrConsumer = 4u, kErrRe
 
 // Call counters in scratch (zero between launches).
 constexpr int kCtlBuilt = 0;     // shared x records built in this call
-constexpr int kCtlDone = 1;      // CTAs finished
-constexpr int kCtlAbort = 2;     // some CTA gave up a wait
+constexpr int kCtlSeen = 1;      // CTAs whose record readers have all seen them complete
 constexpr int kCtlWords = 4;
 
 struct Params {
@@ -175,9 +176,11 @@ struct Params {
     int T;                      // tiles of 128 rows
     int U;                      // T * GP units
     int C;                      // CTAs (grid size)
-    int R;                      // 3 * C ranges
-    int q_units;                // U / R: every range has q_units units, the first rem_units one more
-    int rem_units;              // U % R
+    int R;                      // ranges (at most 3 * C; team j of CTA c runs range 3c + j)
+    int S;                      // ranges per block of L units
+    int L;                      // units per block (U: one block over all tiles; GP: one block per tile)
+    int q_units;                // L / S: every range of a block has q_units units, the first rem_units one more
+    int rem_units;              // L % S
     int build;                  // 1: build the x records here; 0: the preceding glue kernel wrote them
 #ifdef Q4_TRACE
     unsigned long long* trace;  // developer timing trace (compiled in only with Q4_TRACE)
@@ -207,14 +210,25 @@ inline int grid_ctas(int U, int sm_count) {
     return c < sm_count ? c : sm_count;
 }
 
-// Ranges: the first rem ranges have q + 1 units, the others q (q = U / R, rem =
-// U % R), so range r starts at r*q + min(r, rem) -- 32-bit arithmetic only.
-__host__ __device__ __forceinline__ int range_start(int q, int rem, int r) { return r * q + (r < rem ? r : rem); }
+// Ranges.  The U units (unit t*GP + gp: tile t, group pair gp) are cut into
+// blocks of L consecutive units and every block into S ranges, the first rem of
+// them q + 1 units long and the others q (q = L / S >= 1, rem = L % S): range
+// r = b*S + j starts at unit b*L + j*q + min(j, rem), and ranges from R on are
+// empty.  L = U, S = R is stream-K over all tiles (ranges cross tile
+// boundaries); L = GP puts S ranges inside every tile.  32-bit arithmetic, at
+// range boundaries only.
+__host__ __device__ __forceinline__ int range_start(const Params& p, int r) {
+    if (r >= p.R) return p.U;
+    const int b = r / p.S, j = r - b * p.S;
+    return b * p.L + j * p.q_units + (j < p.rem_units ? j : p.rem_units);
+}
 
 // The range that owns unit u (0 <= u < U).
-__device__ __forceinline__ int range_of_unit(int q, int rem, int u) {
-    const int big = (q + 1) * rem;                  // units in the longer ranges
-    return u < big ? u / (q + 1) : rem + (q > 0 ? (u - big) / q : 0);
+__device__ __forceinline__ int range_of_unit(const Params& p, int u) {
+    const int b = u / p.L, v = u - b * p.L;
+    const int q = p.q_units, rem = p.rem_units;
+    const int big = (q + 1) * rem;                  // units in the longer ranges of the block
+    return b * p.S + (v < big ? v / (q + 1) : rem + (v - big) / q);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -282,6 +296,16 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 
 __device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned atom_add_relaxed_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void record_timeout(const Params& p, unsigned int code, volatile int* abort_flag) {
@@ -511,7 +535,7 @@ __device__ __forceinline__ void fold_group(float (&acc)[MT], const uint32_t* P, 
 // y.  Kept out of line (rare); it takes no reference to the caller's sums.
 template <int MT>
 __device__ __noinline__ void finish_tile(const float* __restrict__ partials, float* __restrict__ y, int64_t N, int M,
-                                         int q, int rem, int GP, int t, int row, int r_first, int r_last) {
+                                         int t, int row, int r_first, int r_last, bool first_before) {
     constexpr int W = width<MT>();
     const int64_t n = (int64_t)t * kRowsTile + row;
     float v[MT];
@@ -525,7 +549,9 @@ __device__ __noinline__ void finish_tile(const float* __restrict__ partials, flo
         for (int i = 0; i < kB; ++i) {
             const int rr = rb + i;
             const bool use = rr <= r_last;
-            const int cslot = range_start(q, rem, rr) >= t * GP ? 0 : 1;   // the tile is rr's first segment, or its last
+            // slot 0: the tile is rr's first segment; 1: its last (only r_first can
+            // have started in an earlier tile)
+            const int cslot = (rr == r_first && first_before) ? 1 : 0;
             const float* src = partials + (((int64_t)rr * 2 + cslot) * W) * kRowsTile + row;
 #pragma unroll
             for (int m = 0; m < MT; ++m) pv[i][m] = use ? __ldcg(src + m * kRowsTile) : 0.0f;
@@ -571,8 +597,8 @@ __device__ __forceinline__ void end_segment(const Params& p, float (&acc)[MT], i
         // every lane's reads in finish_tile
         __syncwarp();
         const int tu = t * p.GP;
-        const int r_first = range_of_unit(p.q_units, p.rem_units, tu);
-        const int r_last = range_of_unit(p.q_units, p.rem_units, tu + p.GP - 1);
+        const int r_first = range_of_unit(p, tu);
+        const int r_last = range_of_unit(p, tu + p.GP - 1);
         const int count = r_last - r_first + 1;        // ranges contributing to tile t (none of them empty)
         int last = 0;
         if (lane == 0) {
@@ -586,7 +612,7 @@ __device__ __forceinline__ void end_segment(const Params& p, float (&acc)[MT], i
         }
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
         __syncwarp();
-        if (last) finish_tile<MT>(p.partials, p.y, p.N, p.M, p.q_units, p.rem_units, p.GP, t, row, r_first, r_last);
+        if (last) finish_tile<MT>(p.partials, p.y, p.N, p.M, t, row, r_first, r_last, range_start(p, r_first) < tu);
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
@@ -624,6 +650,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     const int lane = threadIdx.x & 31;
     const int c_id = blockIdx.x;
 
+    if (threadIdx.x == 0) Q4_TMGT(p, c_id, 10);
     // the next kernel on the stream may start now
     pdl_launch_dependents();
 
@@ -676,8 +703,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const int par = weights ? lane % kWeightLanes : (lane - kWL) % kRecordLanes;
         const int step = weights ? kWeightLanes : kRecordLanes;
         const int S = weights ? SN : SR;
-        const int u0 = active ? range_start(p.q_units, p.rem_units, kTeams * c_id + j) : 0;
-        const int nst = active ? range_start(p.q_units, p.rem_units, kTeams * c_id + j + 1) - u0 : 0;
+        const int u0 = active ? range_start(p, kTeams * c_id + j) : 0;
+        const int nst = active ? range_start(p, kTeams * c_id + j + 1) - u0 : 0;
         const int h_loc = p.build ? (nst < H ? nst : H) : 0;     // stages whose records the team builds
         uint64_t* fullb = weights ? fulln + j * SN : fullr + j * SR;
         uint64_t* emptyb = weights ? emptyn + j * SN : emptyr + j * SR;
@@ -711,18 +738,30 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         pdl_wait();
         if (lane == 0) Q4_TMGT(p, c_id, 1);
         bool ok = true;
-        bool records_ok = !p.build;                   // the call's shared records are complete
+        // The shared records of the call: every record lane, and one counting lane,
+        // waits until they are complete; then the CTA counts itself once on
+        // ctl[kCtlSeen], and the last CTA counted returns both counters to zero for
+        // the next call -- all during the call, off its critical path.
+        constexpr int kCountLane = 31;
+        const bool poller = p.build && (lane == kCountLane || (active && !weights));
+        bool records_ok = !poller;                    // this lane has seen the call's records complete
+        bool counted = !p.build;                      // warp-uniform: this CTA is counted
+        unsigned seen_before = 0xFFFFFFFFu;           // the counting lane's ticket
         long long idle_since = clock64();
         while (true) {
             const bool more = active && ok && k < nst;
-            if (!__any_sync(0xFFFFFFFFu, more)) break;
-            if (more && !weights && !records_ok) {
+            if (!__any_sync(0xFFFFFFFFu, more || (ok && !counted))) break;
+            if (ok && !records_ok) {
                 if (ld_acquire_gpu(p.ctl + kCtlBuilt) >= (unsigned)p.G) {
                     // written through the generic proxy, read by the bulk copies through the async one
                     fence_proxy_async_global();
                     records_ok = true;
                     if (lane == kWL) Q4_TMGT(p, c_id, 2);
                 }
+            }
+            if (!counted && __all_sync(0xFFFFFFFFu, records_ok)) {
+                if (lane == kCountLane) seen_before = atom_add_relaxed_gpu(p.ctl + kCtlSeen, 1u);
+                counted = true;
             }
             bool issued = false;
             if (more && (weights || records_ok) &&
@@ -743,6 +782,13 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
                 }
             }
         }
+        // the ticket is read only now, so its round trip never held up a copy; every
+        // other CTA counted has seen the records complete, so nothing reads or adds
+        // to the counters again in this call
+        if (lane == kCountLane && seen_before == (unsigned)p.C - 1) {
+            st_relaxed_gpu(p.ctl + kCtlBuilt, 0u);
+            st_relaxed_gpu(p.ctl + kCtlSeen, 0u);
+        }
         if (!ok && active) {
             // every issued copy must land before the CTA may exit
             const int first = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
@@ -754,8 +800,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     } else if (warp <= kTeams) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
         const int team = warp - 1;
-        const int u0 = range_start(p.q_units, p.rem_units, kTeams * c_id + team);
-        const int nst = range_start(p.q_units, p.rem_units, kTeams * c_id + team + 1) - u0;
+        const int u0 = range_start(p, kTeams * c_id + team);
+        const int nst = range_start(p, kTeams * c_id + team + 1) - u0;
         // first, this CTA's share of the call's x records (groups c, c + C, ...; this
         // warp takes every third of them), counted once written
         if (p.build) {
@@ -774,39 +820,38 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const uint32_t idesc = idesc_bf16_f32(128, 16);
         // B: core matrices K-major, 128 B apart along K, 8-row blocks 1024 B apart
         const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(rec + team * SR * kRecStage + kRecB), 128, 1024);
-        const uint32_t tbase = tmem + (uint32_t)team * kColsTeam;
+        // the tensor-memory base is the same in every lane: take lane 0's, so the
+        // operand arithmetic below is visibly warp-uniform
+        const uint32_t tbase = __shfl_sync(0xFFFFFFFFu, tmem, 0) + (uint32_t)team * kColsTeam;
+        const uint32_t leader = elect_one();           // the lane that issues (and commits) every MMA
         int rs = 0;
         for (int k = 0; k < nst; ++k) {
             // the team hands a stage over only once its records are in shared memory
             if (!__all_sync(0xFFFFFFFFu, wait_or_abort(p, &ready[team], (uint32_t)(k & 1), kErrIssuer, abort_flag)))
                 break;
             tc_fence_after();
-            if (lane == 0) {
-                const uint64_t bd = bdesc0 + (uint64_t)((rs * kRecStage) >> 4);
-                const uint32_t aS = tbase + (a_buffers(W) == 2 ? (uint32_t)(k & 1) * kColsA : 0u);
-                const uint32_t dS = tbase + kColP;
+            const uint64_t bd = bdesc0 + (uint64_t)((rs * kRecStage) >> 4);
+            const uint32_t aS = tbase + (a_buffers(W) == 2 ? (uint32_t)(k & 1) * kColsA : 0u);
+            const uint32_t dS = tbase + kColP;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
-                    // P of group g: columns W*g + m (rows 0-15 in one N = 16 MMA, rows 16-31 in another)
+            for (int g = 0; g < 2; ++g) {
+                const uint64_t bg = bd + (uint64_t)((g * kRec) >> 4);
+                // P of group g: columns W*g + m (rows 0-15 in one N = 16 MMA, rows 16-31 in another)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-                        for (int h = 0; h < W / 16; ++h)
-                            tc_mma_ts(dS + (uint32_t)(W * g + 16 * h), aS + 32u * g + 8u * kk,
-                                      bg + 16u * kk + (uint64_t)(h * (2048 >> 4)), idesc, kk > 0 ? 1u : 0u);
-                    }
+                    for (int h = 0; h < W / 16; ++h)
+                        tc_mma_ts_if(leader, dS + (uint32_t)(W * g + 16 * h), aS + 32u * g + 8u * kk,
+                                     bg + 16u * kk + (uint64_t)(h * (2048 >> 4)), idesc, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(&done[team]);
             }
+            tc_commit_if(leader, &done[team]);
             __syncwarp();
             if (++rs == SR) rs = 0;
         }
         // no MMA of this warp may still run when tensor memory is freed
-        if (lane == 0) {
-            tc_commit(&fin[team]);
-            mbar_wait(&fin[team], 0, kWaitLimit);
-        }
+        tc_commit_if(leader, &fin[team]);
+        if (leader) mbar_wait(&fin[team], 0, kWaitLimit);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ consumer teams
@@ -816,8 +861,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)team * kColsTeam;
         const uint32_t dP = tbase + kColP;
         const int r_id = kTeams * c_id + team;
-        const int u0 = range_start(p.q_units, p.rem_units, r_id);
-        const int nst = range_start(p.q_units, p.rem_units, r_id + 1) - u0;
+        const int u0 = range_start(p, r_id);
+        const int nst = range_start(p, r_id + 1) - u0;
         const int h_loc = p.build ? (nst < H ? nst : H) : 0;
         // shared addresses: this team's first nibble slot (its row), first record
         // slot, first scale/bias buffer (its row's 16 bytes)
@@ -828,6 +873,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
 
         // the predecessor may still read y or the scratch, or produce x
         pdl_wait();
+        if (team == 0 && q == 0 && lane == 0) Q4_TMGT(p, c_id, 14);
         if (h_loc > 0) {
             // the records of the team's first stages, from x, while the call's shared ones are built
             build_records_smem<W, H>(p.x, p.M, p.K, u0 % p.GP, p.GP, h_loc, row,
@@ -835,6 +881,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             fence_proxy_async_smem();                  // for the MMAs (async proxy)
             named_barrier(1 + team, 128);              // every row's X before any warp's fold
         }
+        if (team == 0 && q == 0 && lane == 0) Q4_TMGT(p, c_id, 15);
 
         float acc[MT];
 #pragma unroll
@@ -1002,22 +1049,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0) {
-        Q4_TMGT(p, c_id, 9);
-        // the last CTA of the call returns its counters to zero for the next call
-        if (*abort_flag) atomicOr(p.ctl + kCtlAbort, 1u);
-        unsigned old;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ctl + kCtlDone) : "memory");
-        if (old == (unsigned)p.C - 1) {
-            if (*reinterpret_cast<volatile unsigned*>(p.ctl + kCtlAbort)) {
-                // a CTA that gave up a wait may have skipped tile arrivals
-                for (int i = 0; i < p.R * 4; ++i) p.sems[i] = 0;
-                p.ctl[kCtlAbort] = 0;
-            }
-            p.ctl[kCtlBuilt] = 0;
-            p.ctl[kCtlDone] = 0;
-        }
-    }
+    if (threadIdx.x == 0) Q4_TMGT(p, c_id, 9);
 }
 
 template <int MT>
