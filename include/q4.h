@@ -253,8 +253,9 @@ q4_status q4_check_wait_timeout(long long limit_cycles, q4_stream_t stream);
  * out-of-range codebook id (Q4_ERR_INVALID_INDEX, reported first) or a bounded
  * wait that gave up (Q4_ERR_TIMEOUT) -- then clears that record.  After a wait
  * that gave up it also returns the library's arrival counters to zero (a CTA
- * that gave up may have skipped its arrivals), so later calls start clean.
- * Allocates no device memory.  Q4_OK otherwise. */
+ * that gave up may have skipped its arrivals), so later calls start clean;
+ * results of calls made on that device between the timed-out call and this
+ * query are undefined.  Allocates no device memory.  Q4_OK otherwise. */
 q4_status q4_device_status(q4_stream_t stream);
 
 /* Thread-local description of the last failure on this thread ("" if none). */
