@@ -44,7 +44,10 @@
 //                per stage, L2 evict-first, into the team's nibble ring, and
 //                at the first stage of each block of 8 groups a box of those
 //                rows' scale and bias words), two copy its stages' records
-//                into its record ring.  The lanes run one polling loop.
+//                into its record ring.  The lanes run one polling loop.  Two
+//                stages of weights go out before the preceding kernel has
+//                ended; the rest of the first ring-full only once every team
+//                has loaded its x (which would otherwise queue behind them).
 //   warps 1..3   MMA issuers, one per team: per stage 8 MMAs M128 N16 K16 (16
 //                at W = 32: rows 0-15 and rows 16-31 as two N = 16 MMAs, so a
 //                row's products never depend on the row width), A = the
@@ -107,6 +110,12 @@ __host__ __device__ constexpr int rec_stage_bytes(int W) { return ((2 * rec_byte
 // Stages whose records a team builds itself from x at its start (they do not
 // wait for the call's shared records).
 __host__ __device__ constexpr int local_stages(int W) { return W == 16 ? 3 : 2; }
+// Weight stages per team issued before griddepcontrol.wait.  The rest of the
+// ring's first fill waits until every team has loaded its x: x arrives after the
+// preceding kernel ends and would otherwise queue behind a ring-full of weights
+// on the way into the SM (measured: 0.8 us per attention call).
+constexpr int kEarlyStages = 2;
+static_assert(kEarlyStages <= nib_slots(16) && kEarlyStages <= nib_slots(32), "early stages must find free slots");
 // Producer lanes per team and stream.  A lane issues every L-th stage of its
 // team into a ring of S slots and waits, by phase parity, for the slot's previous
 // user; that wait is unambiguous only while the lane cannot run more than one
@@ -126,6 +135,10 @@ constexpr int kSbBytes = kTeams * kSbBuffers * 2 * kSbBox;      // 24 KB
 static_assert(nib_slots(16) <= 4 * (kSbBuffers - 1) + 1 && nib_slots(32) <= 4 * (kSbBuffers - 1) + 1,
               "a scale/bias buffer could be reloaded while a stage of its block is still unread");
 constexpr int kBarrierBytes = 1024;
+// full/empty per ring slot, ready/done/fin per team, x-ready; then the tensor-memory base and the abort flag
+static_assert((kTeams * (2 * nib_slots(16) + 2 * rec_slots(16)) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes &&
+                  (kTeams * (2 * nib_slots(32) + 2 * rec_slots(32)) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes,
+              "barrier region");
 __host__ __device__ constexpr int smem_bytes_w(int W) {
     return kTeams * (nib_slots(W) * kNibStage + rec_slots(W) * rec_stage_bytes(W)) + kSbBytes + kBarrierBytes +
            1024 /* alignment slack */;
@@ -643,7 +656,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     uint64_t* ready = emptyr + kTeams * SR;                   // [kTeams]: the team's A of a stage stored, its P free
     uint64_t* done = ready + kTeams;                          // [kTeams]: the team's MMAs of a stage complete
     uint64_t* fin = done + kTeams;                            // [kTeams]
-    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kTeams);
+    uint64_t* xrdy = fin + kTeams;                            // every team has loaded its first records' x
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(fin + kTeams + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -668,6 +682,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             mbar_init(&done[i], 1);
             mbar_init(&fin[i], 1);
         }
+        mbar_init(xrdy, kTeams);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -731,9 +746,10 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             }
             k += step;
         };
-        // the weights' first ring-full needs nothing from the preceding kernel
+        // the weights' first stages need nothing from the preceding kernel
         if (active && weights)
-            while (k < nst && k < S) issue();
+            while (k < nst && k < kEarlyStages) issue();
+        bool x_loaded = false;                        // weight lanes: every team has loaded its x
         // the records come from this call (or from the preceding glue kernel)
         pdl_wait();
         if (lane == 0) Q4_TMGT(p, c_id, 1);
@@ -763,8 +779,9 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
                 if (lane == kCountLane) seen_before = atom_add_relaxed_gpu(p.ctl + kCtlSeen, 1u);
                 counted = true;
             }
+            if (weights && !x_loaded) x_loaded = mbar_test_wait(xrdy, 0u);
             bool issued = false;
-            if (more && (weights || records_ok) &&
+            if (more && (weights ? (k < kEarlyStages || x_loaded) : records_ok) &&
                 (k < S || mbar_test_wait(&emptyb[k % S], (uint32_t)(((k / S) & 1) ^ 1)))) {
                 issue();
                 issued = true;
@@ -882,6 +899,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             named_barrier(1 + team, 128);              // every row's X before any warp's fold
         }
         if (team == 0 && q == 0 && lane == 0) Q4_TMGT(p, c_id, 15);
+        if (q == 0 && lane == 0) mbar_arrive(xrdy);   // this team's x loads are done (every team arrives once)
 
         float acc[MT];
 #pragma unroll
