@@ -103,9 +103,12 @@ __host__ __device__ constexpr int rec_b(int W) { return 4 * W; }                
 // Per team: a ring of nibble slots (one 128-row x 64-byte box each, freed as
 // soon as a stage is dequantized) and a ring of record slots (the stage's two x
 // records, freed once its P is folded; the group sums X in them are read by all
-// four warps of the team).
+// four warps of the team).  Both rings have the same depth: stage k uses slot
+// k % depth of each, and one "full" barrier per slot counts the stage's weight
+// box, its scale/bias box and its record copy together, so a consumer waits once
+// per stage.
 __host__ __device__ constexpr int nib_slots(int W) { return W == 16 ? 5 : 4; }
-__host__ __device__ constexpr int rec_slots(int W) { return W == 16 ? 6 : 4; }
+__host__ __device__ constexpr int rec_slots(int W) { return nib_slots(W); }
 __host__ __device__ constexpr int rec_stage_bytes(int W) { return ((2 * rec_bytes(W) + 127) / 128) * 128; }
 // Stages whose records a team builds itself from x at its start (they do not
 // wait for the call's shared records).
@@ -135,9 +138,10 @@ constexpr int kSbBytes = kTeams * kSbBuffers * 2 * kSbBox;      // 24 KB
 static_assert(nib_slots(16) <= 4 * (kSbBuffers - 1) + 1 && nib_slots(32) <= 4 * (kSbBuffers - 1) + 1,
               "a scale/bias buffer could be reloaded while a stage of its block is still unread");
 constexpr int kBarrierBytes = 1024;
-// full/empty per ring slot, ready/done/fin per team, x-ready; then the tensor-memory base and the abort flag
-static_assert((kTeams * (2 * nib_slots(16) + 2 * rec_slots(16)) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes &&
-                  (kTeams * (2 * nib_slots(32) + 2 * rec_slots(32)) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes,
+// full, nibbles-empty, records-empty per ring slot, ready/done/fin per team, x-ready; then the tensor-memory
+// base and the abort flag
+static_assert((kTeams * 3 * nib_slots(16) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes &&
+                  (kTeams * 3 * nib_slots(32) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes,
               "barrier region");
 __host__ __device__ constexpr int smem_bytes_w(int W) {
     return kTeams * (nib_slots(W) * kNibStage + rec_slots(W) * rec_stage_bytes(W)) + kSbBytes + kBarrierBytes +
@@ -649,10 +653,10 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     uint8_t* nib = smem;                                      // [team][SN] nibble boxes
     uint8_t* rec = nib + kTeams * SN * kNibStage;             // [team][SR] two x records each
     uint8_t* sb = rec + kTeams * SR * kRecStage;              // [team][kSbBuffers][plane] scale/bias boxes
-    uint64_t* fulln = reinterpret_cast<uint64_t*>(sb + kSbBytes);   // nibbles (+ scale/bias) landed
+    static_assert(SN == SR, "one full barrier per stage serves both rings");
+    uint64_t* fulln = reinterpret_cast<uint64_t*>(sb + kSbBytes);   // nibbles, scale/bias and records landed
     uint64_t* emptyn = fulln + kTeams * SN;                   // nibble slot read (dequantized)
-    uint64_t* fullr = emptyn + kTeams * SN;                   // records landed
-    uint64_t* emptyr = fullr + kTeams * SR;                   // record slot read (MMAs done, P folded)
+    uint64_t* emptyr = emptyn + kTeams * SN;                  // record slot read (MMAs done, P folded)
     uint64_t* ready = emptyr + kTeams * SR;                   // [kTeams]: the team's A of a stage stored, its P free
     uint64_t* done = ready + kTeams;                          // [kTeams]: the team's MMAs of a stage complete
     uint64_t* fin = done + kTeams;                            // [kTeams]
@@ -674,7 +678,6 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             mbar_init(&emptyn[i], 4);
         }
         for (int i = 0; i < kTeams * SR; ++i) {
-            mbar_init(&fullr[i], 1);
             mbar_init(&emptyr[i], 4);
         }
         for (int i = 0; i < kTeams; ++i) {
@@ -721,7 +724,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const int u0 = active ? range_start(p, kTeams * c_id + j) : 0;
         const int nst = active ? range_start(p, kTeams * c_id + j + 1) - u0 : 0;
         const int h_loc = p.build ? (nst < H ? nst : H) : 0;     // stages whose records the team builds
-        uint64_t* fullb = weights ? fulln + j * SN : fullr + j * SR;
+        uint64_t* fullb = fulln + j * SN;                    // weights and records of a stage land on one barrier
         uint64_t* emptyb = weights ? emptyn + j * SN : emptyr + j * SR;
         int k = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
         if (!active) k = 0;
@@ -731,7 +734,10 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             if (weights) {
                 const int u = u0 + k, t = u / p.GP, gp = u - t * p.GP;
                 const bool sb_new = k == 0 || (u & 3) == 0;
-                mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(kNibStage + (sb_new ? 2 * kSbBox : 0)));
+                // the one arrival of the stage's phase; it also expects the record copy
+                // (stages from h_loc on), which may land before or after it
+                mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(kNibStage + (sb_new ? 2 * kSbBox : 0) +
+                                                               (k >= h_loc ? 2 * kRec : 0)));
                 tma_load_2d_hint(nib + (j * SN + slot) * kNibStage, &map_nib, &fullb[slot], gp * 64, t * kRowsTile, pol);
                 if (sb_new) {
                     const int buf = ((u >> 2) - (u0 >> 2)) % kSbBuffers;
@@ -740,7 +746,6 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
                 }
             } else {
                 const int gp = (u0 + k) % p.GP;
-                mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(2 * kRec));
                 bulk_copy_g2s(rec + (j * SR + slot) * kRecStage, p.xt + (int64_t)(2 * gp) * kRec, (uint32_t)(2 * kRec),
                               &fullb[slot]);
             }
@@ -807,12 +812,11 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             st_relaxed_gpu(p.ctl + kCtlSeen, 0u);
         }
         if (!ok && active) {
-            // every issued copy must land before the CTA may exit
+            // every issued copy must land before the CTA may exit (a stage whose other
+            // part was never issued keeps its phase open: the wait then runs to its limit)
             const int first = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
-            for (int k2 = k - step; k2 >= first && k2 + S >= k; k2 -= step) {
-                const int uses = k2 / S - (!weights && k2 % S < h_loc ? 1 : 0);   // earlier copies into that slot
-                mbar_wait(&fullb[k2 % S], (uint32_t)(uses & 1), kWaitLimit);
-            }
+            for (int k2 = k - step; k2 >= first && k2 + S >= k; k2 -= step)
+                mbar_wait(&fullb[k2 % S], (uint32_t)((k2 / S) & 1), kWaitLimit);
         }
     } else if (warp <= kTeams) {
         // ------------------------------------------------------------ MMA issuers (warp-uniform loop)
@@ -1019,13 +1023,8 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
                 tmem_wait_st();
             }
             tr_mark(1);
-            // the MMAs of this stage read its records, the fold its group sums: a copied
-            // record must have landed before the hand-over (built ones are already there)
-            if (k >= h_loc) {
-                const int uses = k / SR - (rs < h_loc ? 1 : 0);   // earlier copies into this slot
-                live = __all_sync(0xFFFFFFFFu, live && wait_or_abort(p, &fullr[team * SR + rs], (uint32_t)(uses & 1),
-                                                                     kErrConsumer, abort_flag, tr_sp));
-            }
+            // (the stage's records -- copied ones landed on the same barrier as its
+            // weights, built ones were written before the loop -- are in place)
             tr_mark(4);
             // fold the previous stage (its MMAs ran meanwhile); then P is free again
             const bool early = a_buffers(W) == 2 && pend >= 0;
