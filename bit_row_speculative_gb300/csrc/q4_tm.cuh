@@ -57,12 +57,11 @@
 //                share of the call's records.
 //   warps 4..15  three consumer teams of 4 warps, one row per thread.  At
 //                W = 16 a team keeps two A buffers: in its iteration for stage
-//                k it dequantizes stage k into one (and frees its nibble slot
-//                at once) while the MMAs of stage k - 1 run on the other,
-//                loads that stage's P, hands stage k to its issuer, then folds
-//                P into its fp32 sums with s, r and X and frees the record
-//                slot.  At W = 32 (one A buffer, to fit tensor memory) it
-//                folds stage k - 1 first.
+//                k it dequantizes stage k into one while the MMAs of stage
+//                k - 1 run on the other, loads that stage's P, hands stage k
+//                to its issuer, then folds P into its fp32 sums with s, r and
+//                X and frees stage k - 1's slots.  At W = 32 (one A buffer, to
+//                fit tensor memory) it folds stage k - 1 first.
 // Segment ends: a range covers at most two partial tiles (its first and last
 // segments) and whole tiles between.  A warp stores a whole tile's 32 rows to
 // y; for a partial tile it publishes its rows and counts them on the tile's
@@ -100,13 +99,13 @@ template <int MT>
 __host__ __device__ constexpr int width() { return MT > 16 ? 32 : 16; }
 __host__ __device__ constexpr int rec_bytes(int W) { return 4 * W + (W / 8) * 1024; }   // X[W] fp32, then W/8 blocks of 8 rows
 __host__ __device__ constexpr int rec_b(int W) { return 4 * W; }                        // offset of the core matrices
-// Per team: a ring of nibble slots (one 128-row x 64-byte box each, freed as
-// soon as a stage is dequantized) and a ring of record slots (the stage's two x
-// records, freed once its P is folded; the group sums X in them are read by all
-// four warps of the team).  Both rings have the same depth: stage k uses slot
-// k % depth of each, and one "full" barrier per slot counts the stage's weight
-// box, its scale/bias box and its record copy together, so a consumer waits once
-// per stage.
+// Per team: a ring of nibble slots (one 128-row x 64-byte box each) and a ring
+// of record slots (the stage's two x records; the group sums X in them are read
+// by all four warps of the team), of the same depth: stage k uses slot k % depth
+// of each.  One "full" barrier per slot counts the stage's weight box, its
+// scale/bias box and its record copy together, and one "empty" barrier frees
+// both slots once the stage's P is folded, so a consumer warp makes one wait
+// and one arrival per stage on the ring (each costs a round trip).
 __host__ __device__ constexpr int nib_slots(int W) { return W == 16 ? 5 : 4; }
 __host__ __device__ constexpr int rec_slots(int W) { return nib_slots(W); }
 __host__ __device__ constexpr int rec_stage_bytes(int W) { return ((2 * rec_bytes(W) + 127) / 128) * 128; }
@@ -129,19 +128,19 @@ constexpr int kRecordLanes = 2;
 // Scale and bias words: per team two buffers (blocks of 8 groups = 4 stages),
 // each a 128-row x 16-byte box of the scale plane and one of the bias plane.  A
 // buffer is reloaded at the first stage of the block after next, which the
-// producer issues only once the nibble slot of the stage nib_slots earlier has
-// been freed: at most 5 slots keep that stage at or after the last stage of the
-// block the buffer held.
+// producer issues only once the slots of the stage nib_slots earlier have been
+// freed (that stage folded): at most 5 slots keep that stage at or after the
+// last stage of the block the buffer held.
 constexpr int kSbBuffers = 2;
 constexpr int kSbBox = kRowsTile * 16;                          // 2 KB
 constexpr int kSbBytes = kTeams * kSbBuffers * 2 * kSbBox;      // 24 KB
 static_assert(nib_slots(16) <= 4 * (kSbBuffers - 1) + 1 && nib_slots(32) <= 4 * (kSbBuffers - 1) + 1,
               "a scale/bias buffer could be reloaded while a stage of its block is still unread");
 constexpr int kBarrierBytes = 1024;
-// full, nibbles-empty, records-empty per ring slot, ready/done/fin per team, x-ready; then the tensor-memory
-// base and the abort flag
-static_assert((kTeams * 3 * nib_slots(16) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes &&
-                  (kTeams * 3 * nib_slots(32) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes,
+// full and empty per ring slot, ready/done/fin per team, x-ready; then the tensor-memory base and the
+// abort flag
+static_assert((kTeams * 2 * nib_slots(16) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes &&
+                  (kTeams * 2 * nib_slots(32) + 3 * kTeams + 1) * 8 + 8 <= kBarrierBytes,
               "barrier region");
 __host__ __device__ constexpr int smem_bytes_w(int W) {
     return kTeams * (nib_slots(W) * kNibStage + rec_slots(W) * rec_stage_bytes(W)) + kSbBytes + kBarrierBytes +
@@ -655,8 +654,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     uint8_t* sb = rec + kTeams * SR * kRecStage;              // [team][kSbBuffers][plane] scale/bias boxes
     static_assert(SN == SR, "one full barrier per stage serves both rings");
     uint64_t* fulln = reinterpret_cast<uint64_t*>(sb + kSbBytes);   // nibbles, scale/bias and records landed
-    uint64_t* emptyn = fulln + kTeams * SN;                   // nibble slot read (dequantized)
-    uint64_t* emptyr = emptyn + kTeams * SN;                  // record slot read (MMAs done, P folded)
+    uint64_t* emptyr = fulln + kTeams * SN;                   // the stage's slots read (MMAs done, P folded)
     uint64_t* ready = emptyr + kTeams * SR;                   // [kTeams]: the team's A of a stage stored, its P free
     uint64_t* done = ready + kTeams;                          // [kTeams]: the team's MMAs of a stage complete
     uint64_t* fin = done + kTeams;                            // [kTeams]
@@ -675,7 +673,6 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int i = 0; i < kTeams * SN; ++i) {
             mbar_init(&fulln[i], 1);
-            mbar_init(&emptyn[i], 4);
         }
         for (int i = 0; i < kTeams * SR; ++i) {
             mbar_init(&emptyr[i], 4);
@@ -725,7 +722,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         const int nst = active ? range_start(p, kTeams * c_id + j + 1) - u0 : 0;
         const int h_loc = p.build ? (nst < H ? nst : H) : 0;     // stages whose records the team builds
         uint64_t* fullb = fulln + j * SN;                    // weights and records of a stage land on one barrier
-        uint64_t* emptyb = weights ? emptyn + j * SN : emptyr + j * SR;
+        uint64_t* emptyb = emptyr + j * SR;                  // both slots of a stage are freed together
         int k = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
         if (!active) k = 0;
         const uint64_t pol = policy_evict_first();
@@ -1013,9 +1010,6 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             const uint32_t nb = nib0 + (uint32_t)(ns * kNibStage);
             const uint4 w0 = lds128(nb + ((0 ^ sx) << 4)), w1 = lds128(nb + ((1 ^ sx) << 4));
             const uint4 w2 = lds128(nb + ((2 ^ sx) << 4)), w3 = lds128(nb + ((3 ^ sx) << 4));
-            // the nibbles (and this stage's scale/bias words) are in registers: the slot may refill
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&emptyn[team * SN + ns]);
             if (live) {
                 const uint32_t aA = tbase + (a_buffers(W) == 2 ? (uint32_t)(k & 1) * kColsA : 0u);
                 dequant64_store(w0, w1, cc0, aA);
