@@ -464,19 +464,21 @@ __device__ __forceinline__ void build_records_smem(const uint16_t* __restrict__ 
     }
 }
 
-// Dequantize the 64 nibbles of one row and group (two 16-byte chunks) into 32
-// bf16 pairs, (q - c) * 2^-133 for the even inputs and (q - c) * 2^-129 for the
-// odd ones, word order (k0,k4) (k1,k5) (k2,k6) (k3,k7) per 8 inputs, and store
-// them to tensor-memory columns taddr .. taddr + 31 of the thread's lane.  Each
-// block of two nibble words (8 columns) is one PTX sequence -- shift, AND, bf16x2
-// subtraction, store -- so its 8 results are formed in the store's registers.
-// cc0 = c * 0x00010001 (c * 2^-133 as a bf16 pair), cc1 = cc0 << 4.
-__device__ __forceinline__ void dequant16_store(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t cc0, uint32_t cc1) {
+// Dequantize 32 nibbles of one row (four nibble words) into 16 bf16 pairs,
+// (q - c) * 2^-133 for the even inputs and (q - c) * 2^-129 for the odd ones,
+// word order (k0,k4) (k1,k5) (k2,k6) (k3,k7) per 8 inputs, and store them to
+// tensor-memory columns taddr .. taddr + 15 of the thread's lane.  One PTX
+// sequence -- shift, AND, bf16x2 subtraction, one 16-column store -- so the
+// results are formed in the store's registers.  cc0 = c * 0x00010001 (c * 2^-133
+// as a bf16 pair), cc1 = cc0 << 4.
+__device__ __forceinline__ void dequant32_store(uint32_t taddr, const uint4& n, uint32_t cc0, uint32_t cc1) {
     asm volatile(
         "{\n\t"
-        ".reg .b32 u0, u1, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
+        ".reg .b32 u0, u1, u2, u3, a0, a1, a2, a3, a4, a5, a6, a7, a8, a9, a10, a11, a12, a13, a14, a15;\n\t"
         "shr.b32 u0, %1, 8;\n\t"
         "shr.b32 u1, %2, 8;\n\t"
+        "shr.b32 u2, %3, 8;\n\t"
+        "shr.b32 u3, %4, 8;\n\t"
         "and.b32 a0, %1, 0x000F000F;\n\t"
         "and.b32 a1, %1, 0x00F000F0;\n\t"
         "and.b32 a2, u0, 0x000F000F;\n\t"
@@ -485,41 +487,59 @@ __device__ __forceinline__ void dequant16_store(uint32_t taddr, uint32_t v0, uin
         "and.b32 a5, %2, 0x00F000F0;\n\t"
         "and.b32 a6, u1, 0x000F000F;\n\t"
         "and.b32 a7, u1, 0x00F000F0;\n\t"
-        "sub.rn.bf16x2 a0, a0, %3;\n\t"
-        "sub.rn.bf16x2 a1, a1, %4;\n\t"
-        "sub.rn.bf16x2 a2, a2, %3;\n\t"
-        "sub.rn.bf16x2 a3, a3, %4;\n\t"
-        "sub.rn.bf16x2 a4, a4, %3;\n\t"
-        "sub.rn.bf16x2 a5, a5, %4;\n\t"
-        "sub.rn.bf16x2 a6, a6, %3;\n\t"
-        "sub.rn.bf16x2 a7, a7, %4;\n\t"
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {a0, a1, a2, a3, a4, a5, a6, a7};\n\t"
+        "and.b32 a8, %3, 0x000F000F;\n\t"
+        "and.b32 a9, %3, 0x00F000F0;\n\t"
+        "and.b32 a10, u2, 0x000F000F;\n\t"
+        "and.b32 a11, u2, 0x00F000F0;\n\t"
+        "and.b32 a12, %4, 0x000F000F;\n\t"
+        "and.b32 a13, %4, 0x00F000F0;\n\t"
+        "and.b32 a14, u3, 0x000F000F;\n\t"
+        "and.b32 a15, u3, 0x00F000F0;\n\t"
+        "sub.rn.bf16x2 a0, a0, %5;\n\t"
+        "sub.rn.bf16x2 a1, a1, %6;\n\t"
+        "sub.rn.bf16x2 a2, a2, %5;\n\t"
+        "sub.rn.bf16x2 a3, a3, %6;\n\t"
+        "sub.rn.bf16x2 a4, a4, %5;\n\t"
+        "sub.rn.bf16x2 a5, a5, %6;\n\t"
+        "sub.rn.bf16x2 a6, a6, %5;\n\t"
+        "sub.rn.bf16x2 a7, a7, %6;\n\t"
+        "sub.rn.bf16x2 a8, a8, %5;\n\t"
+        "sub.rn.bf16x2 a9, a9, %6;\n\t"
+        "sub.rn.bf16x2 a10, a10, %5;\n\t"
+        "sub.rn.bf16x2 a11, a11, %6;\n\t"
+        "sub.rn.bf16x2 a12, a12, %5;\n\t"
+        "sub.rn.bf16x2 a13, a13, %6;\n\t"
+        "sub.rn.bf16x2 a14, a14, %5;\n\t"
+        "sub.rn.bf16x2 a15, a15, %6;\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {a0, a1, a2, a3, a4, a5, a6, a7, a8, a9, a10, a11, a12, a13, "
+        "a14, a15};\n\t"
         "}" ::"r"(taddr),
-        "r"(v0), "r"(v1), "r"(cc0), "r"(cc1)
+        "r"(n.x), "r"(n.y), "r"(n.z), "r"(n.w), "r"(cc0), "r"(cc1)
         : "memory");
 }
 
 __device__ __forceinline__ void dequant64_store(const uint4& n0, const uint4& n1, uint32_t cc0, uint32_t taddr) {
     const uint32_t cc1 = cc0 << 4;
-    dequant16_store(taddr, n0.x, n0.y, cc0, cc1);
-    dequant16_store(taddr + 8u, n0.z, n0.w, cc0, cc1);
-    dequant16_store(taddr + 16u, n1.x, n1.y, cc0, cc1);
-    dequant16_store(taddr + 24u, n1.z, n1.w, cc0, cc1);
+    dequant32_store(taddr, n0, cc0, cc1);
+    dequant32_store(taddr + 16u, n1, cc0, cc1);
 }
 
 // Constants of one row and group from its bf16 scale and bias (the low 16
 // bits of s_bits / b_bits): c = clamp(rint(-b/s), 0, 15) (NaN -> 0),
-// r = b + c*s, s * 2^33 and the bf16 pair c * 2^-133.
+// r = b + c*s, s * 2^33 and the bf16 pair c * 2^-133.  t = 1.5 * 2^23 - b/s
+// holds rint(-b/s) in its low mantissa bits (the fp32 addition rounds to the
+// nearest integer, ties to even); clamped in that form, its low byte is c.
+// Any c in 0..15 keeps q - c exact; rint(-b/s) only keeps s*P and r*X small.
 __device__ __forceinline__ void group_constants(uint32_t s_bits, uint32_t b_bits, float& s_fold, float& r,
                                                 uint32_t& cc0) {
+    constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23
     const float s = __uint_as_float(s_bits << 16);
     const float b = __uint_as_float(b_bits << 16);
-    float cf = rintf(__fdividef(-b, s));
-    cf = fminf(fmaxf(cf, 0.0f), 15.0f);
-    r = __fmaf_rn(cf, s, b);
+    float t = __fmaf_rn(-b, __fdividef(1.0f, s), kMagic);
+    t = fminf(fmaxf(t, kMagic), kMagic + 15.0f);
+    r = __fmaf_rn(t - kMagic, s, b);
     s_fold = s * kFoldScale;
-    const uint32_t ci = __float_as_uint(__fadd_rn(8388608.0f, cf)) & 0xFu;   // low bits of 2^23 + c
-    cc0 = ci * 0x00010001u;
+    cc0 = prmt(__float_as_uint(t), 0u, 0x4040u);   // (c, c) as a bf16 pair of c * 2^-133
 }
 
 // acc[m] = fma(s, P[m], fma(r, X[m], acc[m])) for m < MT, the same two
@@ -667,6 +687,13 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
     const int c_id = blockIdx.x;
 
     if (threadIdx.x == 0) Q4_TMGT(p, c_id, 10);
+#ifdef Q4_TRACE
+    if (threadIdx.x == 0 && p.trace) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[c_id * 32 + 25] = smid;
+    }
+#endif
     // the next kernel on the stream may start now
     pdl_launch_dependents();
 
@@ -936,7 +963,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         auto arrive_ready = [&]() {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ready[team]);
+            mbar_arrive_elected(&ready[team]);
         };
         // fold the pending stage (signal_ready: hand the current stage over as
         // soon as P is in registers), free its record slot, close its segment if it ends one
@@ -978,10 +1005,11 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             } else if (signal_ready) {
                 arrive_ready();
             }
-            // that stage's records have been read (by the MMAs and the fold), and so has P
+            // that stage's records have been read (by the MMAs and the fold: every value
+            // it loaded has been used), and so has P
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&emptyr[team * SR + pend_rs]);
+            mbar_arrive_relaxed_elected(&emptyr[team * SR + pend_rs]);
             tr_mark(3);
             if (pend_gp == p.GP - 1 || pend == nst - 1) {
                 const bool whole = seg_first_gp == 0 && pend_gp == p.GP - 1;
