@@ -132,6 +132,7 @@ constexpr int kRecordLanes = 2;
 // freed (that stage folded): at most 5 slots keep that stage at or after the
 // last stage of the block the buffer held.
 constexpr int kSbBuffers = 2;
+static_assert((kSbBuffers & (kSbBuffers - 1)) == 0, "buffer index by mask");
 constexpr int kSbBox = kRowsTile * 16;                          // 2 KB
 constexpr int kSbBytes = kTeams * kSbBuffers * 2 * kSbBox;      // 24 KB
 static_assert(nib_slots(16) <= 4 * (kSbBuffers - 1) + 1 && nib_slots(32) <= 4 * (kSbBuffers - 1) + 1,
@@ -752,28 +753,43 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
         uint64_t* emptyb = emptyr + j * SR;                  // both slots of a stage are freed together
         int k = weights ? par : h_loc + ((par - h_loc) % step + step) % step;
         if (!active) k = 0;
+        // the tile and group pair of this lane's next stage, advanced by step (< GP)
+        // per issue: no division in the loop
+        int cur_t = (u0 + k) / p.GP, cur_gp = (u0 + k) - cur_t * p.GP;
+        int slot = k % S;
+        uint32_t ph = (uint32_t)((k / S) & 1);       // phase of this lane's next stage in its slot
         const uint64_t pol = policy_evict_first();
         auto issue = [&]() {
-            const int slot = k % S;
+            const int t = cur_t, gp = cur_gp;
             if (weights) {
-                const int u = u0 + k, t = u / p.GP, gp = u - t * p.GP;
-                const bool sb_new = k == 0 || (u & 3) == 0;
+                const int u = u0 + k;
+                const bool sb_new = k == 0 || (gp & 3) == 0;   // GP is a multiple of 4
                 // the one arrival of the stage's phase; it also expects the record copy
                 // (stages from h_loc on), which may land before or after it
                 mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(kNibStage + (sb_new ? 2 * kSbBox : 0) +
                                                                (k >= h_loc ? 2 * kRec : 0)));
                 tma_load_2d_hint(nib + (j * SN + slot) * kNibStage, &map_nib, &fullb[slot], gp * 64, t * kRowsTile, pol);
                 if (sb_new) {
-                    const int buf = ((u >> 2) - (u0 >> 2)) % kSbBuffers;
+                    const int buf = ((u >> 2) - (u0 >> 2)) & (kSbBuffers - 1);
                     tma_load_3d_hint(sb + (j * kSbBuffers + buf) * 2 * kSbBox, &map_sb, &fullb[slot], 8 * (gp >> 2),
                                      t * kRowsTile, 0, pol);
                 }
             } else {
-                const int gp = (u0 + k) % p.GP;
+                (void)t;
                 bulk_copy_g2s(rec + (j * SR + slot) * kRecStage, p.xt + (int64_t)(2 * gp) * kRec, (uint32_t)(2 * kRec),
                               &fullb[slot]);
             }
             k += step;
+            cur_gp += step;
+            if (cur_gp >= p.GP) {
+                cur_gp -= p.GP;
+                ++cur_t;
+            }
+            slot += step;
+            if (slot >= S) {                          // step < S: one wrap at most
+                slot -= S;
+                ph ^= 1u;
+            }
         };
         // the weights' first stages need nothing from the preceding kernel
         if (active && weights)
@@ -811,7 +827,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             if (weights && !x_loaded) x_loaded = mbar_test_wait(xrdy, 0u);
             bool issued = false;
             if (more && (weights ? (k < kEarlyStages || x_loaded) : records_ok) &&
-                (k < S || mbar_test_wait(&emptyb[k % S], (uint32_t)(((k / S) & 1) ^ 1)))) {
+                (k < S || mbar_test_wait(&emptyb[slot], ph ^ 1u))) {
                 issue();
                 issued = true;
             }
@@ -994,13 +1010,12 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
                     if (signal_ready) arrive_ready();
                     fold_group<MT>(acc, P, xs1, ps1, pr1);
                 } else {
-                    uint32_t P0[16], P1[16];
-                    tmem_ld_32x32b_x16(dP, P0);
-                    tmem_ld_32x32b_x16(dP + 16u, P1);
+                    uint32_t P[32];                    // both groups' 16 columns, one load
+                    tmem_ld_32x32b_x32(dP, P);
                     tmem_wait_ld();
                     if (signal_ready) arrive_ready();
-                    fold_group<MT>(acc, P0, xs0, ps0, pr0);
-                    fold_group<MT>(acc, P1, xs1, ps1, pr1);
+                    fold_group<MT>(acc, P, xs0, ps0, pr0);
+                    fold_group<MT>(acc, P + 16, xs1, ps1, pr1);
                 }
             } else if (signal_ready) {
                 arrive_ready();
@@ -1027,7 +1042,7 @@ q4_tm_kernel(const __grid_constant__ CUtensorMap map_nib, const __grid_constant_
             tr_mark(0);
             if (k == 0 && q == 0 && lane == 0) Q4_TMGT(p, c_id, 3 + team);
             // scale and bias of this stage's two groups: word st_gp % 4 of the buffer of its block
-            const int sbuf = (((u0 + k) >> 2) - (u0 >> 2)) % kSbBuffers;
+            const int sbuf = (((u0 + k) >> 2) - (u0 >> 2)) & (kSbBuffers - 1);
             const uint32_t a = sb_row + (uint32_t)(sbuf * 2 * kSbBox + (st_gp & 3) * 4);
             const uint32_t sw = lds32(a), bw = lds32(a + kSbBox);
             uint32_t cc0, cc1;
