@@ -438,6 +438,8 @@ q4_status check_glue_args(const float* y, int M, int64_t n_prev, int64_t K, int 
     } else {
         return fail(Q4_ERR_INVALID_ARG, "unknown glue kind %d", kind);
     }
+    // the kernel's slices are whole groups of 64 inputs (K_next is the K of a matmul)
+    if (K % 64 != 0) return fail(Q4_ERR_UNSUPPORTED_SHAPE, "K_next = %lld must be a multiple of 64", (long long)K);
     if (!aligned16(y) || !aligned16(x))
         return fail(Q4_ERR_MISALIGNED, "y and x must be 16-byte aligned (y=%p x=%p)", (const void*)y, x);
     return Q4_OK;

@@ -154,10 +154,11 @@ typedef struct {
 } q4_layer;
 
 /* The inter-layer step alone: x_next[M, K_next] (bf16, device) from y[M, N_prev]
- * (fp32, device), as described above.  Both 16-byte aligned.  Asynchronous on
- * `stream`; the kernel waits for the preceding kernel on the stream (it may be
- * the matmul that writes y).  Provided so that a chained pass can be run and
- * checked one layer at a time. */
+ * (fp32, device), as described above.  Both 16-byte aligned.  K_next: a
+ * multiple of 64 (the K of the next matmul), else Q4_ERR_UNSUPPORTED_SHAPE.
+ * Asynchronous on `stream`; the kernel waits for the preceding kernel on the
+ * stream (it may be the matmul that writes y).  Provided so that a chained
+ * pass can be run and checked one layer at a time. */
 q4_status q4_glue(const float* y, int M, int64_t N_prev, int64_t K_next, int glue, void* x_next,
                   q4_stream_t stream);
 

@@ -117,6 +117,7 @@ def test_decode_step_rejects_bad_lists_before_launch(spec, ws, status):
     (4, 640, 300, q4.GLUE_SWIGLU_RMSNORM, q4.Q4_ERR_INVALID_ARG),       # N_prev != 2K
     (4, 640, 320, 3, q4.Q4_ERR_INVALID_ARG),                            # unknown kind
     (0, 640, 320, q4.GLUE_RMSNORM, q4.Q4_ERR_INVALID_ARG),              # M = 0
+    (4, 640, 100, q4.GLUE_RMSNORM, q4.Q4_ERR_UNSUPPORTED_SHAPE),        # K not a multiple of 64
 ])
 def test_glue_rejects_bad_arguments(M, n_prev, K, kind, status):
     lib = q4.lib()

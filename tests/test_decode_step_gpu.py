@@ -120,10 +120,13 @@ def test_glue_rows_are_independent():
 
 
 def _small_chain(device="cuda"):
-    """Four layers with both glue kinds, a K that is not a multiple of 512 (the
-    generic kernel) and ragged N."""
-    spec = [(2048, 512, q4.GLUE_SWIGLU_RMSNORM), (1280, 1024, q4.GLUE_RMSNORM), (1024, 576, q4.GLUE_RMSNORM),
-            (300, 1024, q4.GLUE_NONE)]
+    """Five layers: both glue kinds between two tensor-memory matmuls (formed
+    inside the matmul kernels; the second from a ragged N = 1100 whose first
+    1024 outputs feed the next layer), a K that is not a multiple of 512 (the
+    generic kernel: the glue kernel writes its x, then the next matmul's
+    records) and a ragged last N."""
+    spec = [(2048, 512, q4.GLUE_SWIGLU_RMSNORM), (1100, 1024, q4.GLUE_RMSNORM), (1280, 1024, q4.GLUE_RMSNORM),
+            (1024, 576, q4.GLUE_RMSNORM), (300, 1024, q4.GLUE_NONE)]
     return [(si.make_weights(N, K, 900 + i, device=device), N, K, g) for i, (N, K, g) in enumerate(spec)]
 
 
