@@ -83,6 +83,11 @@ uint64_t q4_packed_bytes(uint64_t N, uint64_t K);
  * this scratch, so calls that may run at the same time on one device (different
  * streams without an ordering between them) race and give wrong results: order
  * them on one stream or with events.
+ * Ordering: the kernel is launched with programmatic dependent launch.  It
+ * loads the first boxes of W before the preceding kernel on `stream` has
+ * finished; x, y and the scratch only afterwards.  So W must not be written by
+ * a preceding kernel that lets its dependents start early
+ * (griddepcontrol.launch_dependents): ordinary kernels finish first.
  * Residency: the kernel runs one CTA per SM and its CTAs exchange the call's x
  * records, so all of them must be resident at once.  A context that gets fewer
  * SMs than the device reports (an MPS client limited to a share of the SMs, for
