@@ -445,7 +445,8 @@ q4_status check_glue_args(const float* y, int M, int64_t n_prev, int64_t K, int 
     return Q4_OK;
 }
 
-// One cluster of glue::slices(K) CTAs per row, chained by programmatic dependent launch.
+// glue::slices(K) CTAs per row (a cluster, unless every CTA sums its row alone), chained by
+// programmatic dependent launch.
 // x mode (rec == nullptr): x_next bf16 [M, K] to x.  Record mode: the next
 // matmul's x records (row width rec_w) to rec instead.
 q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind, void* x, cudaStream_t stream,
@@ -464,8 +465,10 @@ q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, q4::glue::glue_kernel, y, n_prev, K, kind, kGlueEps,
+    cfg.numAttrs = q4::glue::one_cta_rows(kind, K) ? 1 : 2;   // rows a CTA sums alone need no cluster
+    const float eps_hi = (float)kGlueEps;
+    const float eps_lo = (float)(kGlueEps - (double)eps_hi);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, q4::glue::glue_kernel, y, n_prev, K, kind, eps_hi, eps_lo,
                                        static_cast<uint16_t*>(x), rec, rec_w);
     if (e != cudaSuccess) return cuda_fail(e, "launching the glue kernel");
     return Q4_OK;

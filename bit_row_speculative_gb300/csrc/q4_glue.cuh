@@ -9,10 +9,13 @@
 // norms) are not on the matmul path; this fixed, bounded stand-in keeps the
 // values of a long chain of linears in range.
 //
-// Work split: one thread-block cluster per row, S = slices(K) CTAs (at most 8)
-// each owning a contiguous slice of the row made of whole groups of 64 inputs,
-// so a step's glue runs on up to 8*M SMs instead of M.  S and the slices
-// depend on K only.
+// Work split: S = slices(K) CTAs per row (at most 8), each writing the outputs
+// of a contiguous slice of the row made of whole groups of 64 inputs, so a
+// step's glue runs on up to 8*M SMs instead of M.  S and the slices depend on K
+// only.  RMSNORM rows of at most 6144 inputs: every CTA forms the whole row's
+// sum of squares itself (thread t: 8-input blocks t, t + 256, t + 512), so no
+// CTA waits for another.  Otherwise the S CTAs of a row form a cluster and
+// each sums its own slice (the order below).
 //
 // Two outputs.  x mode writes x_next as bf16 [M, K].  Record mode (inside a
 // chained pass, when the next matmul runs the tensor-memory kernel) writes the
@@ -24,12 +27,14 @@
 // single-precision pipes.  The sum of squares is kept as an unevaluated pair of
 // floats (each square split exactly by an fma, the pairs added with error-free
 // two-sums), which carries about 48 significant bits.  Each thread takes 8-input
-// blocks (t, t + 256, ... of its slice) and adds their squares in increasing k;
-// the threads' sums go through a fixed tree over lanes and warps; the slices
-// are combined in cluster-rank order through distributed shared memory, and the
-// scale 1/sqrt(ss/K + eps) is formed in double and split into two floats.  y is
-// read once: a thread's first two blocks stay in registers for the outputs (all
-// of a slice up to 4096 inputs).
+// blocks (t, t + 256, ... of the row, or of its slice in a cluster) and adds their
+// squares in increasing k; the threads' sums go through a fixed tree over lanes
+// and warps; in a cluster the slices are combined in rank order through
+// distributed shared memory (their sums fetched together).  The scale
+// 1/sqrt(ss/K + eps) is formed as a float pair (one Newton step from the float
+// value; relative error below 3e-14).  y is read once per CTA: a thread's first
+// blocks stay in registers for the outputs (all of a slice up to 4096 inputs,
+// or of a row up to 6144).
 //   RMSNORM: v is an exact float, so v * scale is formed as a normalised float
 //   pair and rounded to bf16 from it (the dropped 16 bits of the high part, and
 //   at an exact float midpoint the sign of the low part): the rounding of the
@@ -42,7 +47,7 @@
 //   a pair division; about 1e-14) and rounded from the pair.  Its sum of squares
 //   is over the fp32 values, so its scale is within about 5e-7 of an all-double
 //   one (typically 1e-8).
-// No double arithmetic per element.  Each row's result depends on that row and
+// No double arithmetic.  Each row's result depends on that row and
 // K alone.
 // Programmatic dependent launch: the kernel lets the next kernel start at once
 // and reads y only after the preceding kernel finished.  The cluster barrier is
@@ -68,6 +73,13 @@ constexpr int64_t kSliceMin = 1024;           // inputs per slice below which fe
 // bf16 rounding drops) are within this many float ulps of the halfway point.
 constexpr int kTieMarginSwiglu = 10;          // SWIGLU: the fp32 output is within 9 float ulps of exact
 constexpr int kKeep = 2;                      // 8-input blocks per thread held in registers (slices <= 4096 inputs)
+
+// RMSNORM rows of at most kRowMax inputs: every CTA of the row forms the row's sum
+// of squares itself, kRowKeep 8-input blocks per thread (no cluster).
+constexpr int kRowKeep = 3;
+constexpr int64_t kRowMax = (int64_t)kRowKeep * kThreads * 8;   // 6144
+
+__host__ __device__ inline bool one_cta_rows(int kind, int64_t K) { return kind == 1 && K <= kRowMax; }
 
 inline int slices(int64_t K) {
     int64_t s = (K + kSliceMin - 1) / kSliceMin;
@@ -165,29 +177,145 @@ __device__ __forceinline__ float value_f(float a, float b, int kind) {
     return kind == 2 ? a / (1.0f + expf(-a)) * b : a;
 }
 
+// The scale 1/sqrt(ss/K + eps) of a row from its sum of squares th + tl, as a
+// float pair: one Newton step from the correctly rounded float reciprocal square
+// root (relative error below 3e-14, checked on the CPU against 40-digit
+// arithmetic).  eps_hi + eps_lo: eps as a float pair.
+__device__ __forceinline__ fpair row_scale(float th, float tl, int64_t K, float eps_hi, float eps_lo) {
+    fpair t = pair_div_f(fast_two_sum(th, tl), (float)K);
+    t = pair_add(t, fpair{eps_hi, eps_lo});
+    const float r0 = __fdiv_rn(1.0f, __fsqrt_rn(t.hi));
+    const float q = __fmul_rn(r0, r0);
+    const fpair tr = pair_mul(t, fpair{q, __fmaf_rn(r0, r0, -q)});   // t * r0^2, close to 1
+    const fpair e = pair_add(fpair{1.0f, 0.0f}, fpair{-tr.hi, -tr.lo});
+    return fast_two_sum(r0, __fmul_rn(__fmul_rn(0.5f, r0), __fadd_rn(e.hi, e.lo)));
+}
+
 // x: bf16 [M, K] (x mode) or nullptr; rec: the next matmul's records [K/64][rec_bytes(rec_w)] (record mode) or nullptr.
+// grid (S, M); a cluster of the S CTAs of a row unless one_cta_rows(kind, K).
 __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict__ y, int64_t n_prev, int64_t K,
-                                                        int kind, double eps, uint16_t* __restrict__ x,
+                                                        int kind, float eps_hi, float eps_lo, uint16_t* __restrict__ x,
                                                         uint8_t* __restrict__ rec, int rec_w) {
     namespace cg = cooperative_groups;
     __shared__ float part_hi[kThreads / 32], part_lo[kThreads / 32];
     __shared__ float slice_sum[2];
-    __shared__ double inv_s;
+    __shared__ float inv_s[2];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");     // y comes from the preceding kernel
-    cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)gridDim.x;
     const int s = (int)blockIdx.x;
     const int m = (int)blockIdx.y;
     const int64_t L = (K / 64 + S - 1) / S * 64;     // whole groups
     const int64_t k0 = (int64_t)s * L;
     const int64_t k1 = (k0 + L < K) ? k0 + L : K;
-    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8; // 8-input blocks of this slice; thread t takes t, t + 256, ...
     const float* yr = y + (int64_t)m * n_prev;
     const bool vec = (n_prev & 3) == 0;              // rows 16-byte aligned
 
-    // 1. the sum of squares: each thread's blocks in increasing k; the first kKeep blocks
-    //    stay in registers for step 2 (all their loads in flight together)
+    // The block of inputs kb .. kb+7 (of this CTA's slice when active): its 8 outputs
+    // to x, or into the next matmul's records (uniform over the CTA: whole warps call it).
+    const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
+    auto emit = [&](int64_t kb, bool active, const float (&a)[8], const float (&bv)[8], float inv_f, float inv_lo) {
+        uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (active) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                h[e] = output_bits(value_f(a[e], bv[e], kind), a[e], bv[e], kind, inv_f, inv_lo);
+        }
+        if (rec == nullptr) {
+            if (active) {
+                uint4 o;
+                o.x = h[0] | (h[1] << 16);
+                o.y = h[2] | (h[3] << 16);
+                o.z = h[4] | (h[5] << 16);
+                o.w = h[6] | (h[7] << 16);
+                *reinterpret_cast<uint4*>(x + (int64_t)m * K + kb) = o;
+            }
+            return;
+        }
+        // record mode: the group sum X, the 8 values in increasing k, then the 8 blocks of the
+        // group (8 consecutive lanes, all active or none: slices are whole groups) by a fixed xor tree
+        float sx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sx = __fadd_rn(sx, __uint_as_float(h[e] << 16));
+        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 1));
+        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 2));
+        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 4));
+        if (active) {
+            const int64_t g = kb / 64;
+            const int kc = (int)((kb / 8) & 7);
+            uint8_t* r = rec + g * rb;
+            uint4 o;                                  // pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), scaled
+            o.x = q4::tm::bf16x2_mul(h[0] | (h[4] << 16), q4::tm::kXScaleEven);
+            o.y = q4::tm::bf16x2_mul(h[1] | (h[5] << 16), q4::tm::kXScaleOdd);
+            o.z = q4::tm::bf16x2_mul(h[2] | (h[6] << 16), q4::tm::kXScaleEven);
+            o.w = q4::tm::bf16x2_mul(h[3] | (h[7] << 16), q4::tm::kXScaleOdd);
+            *reinterpret_cast<uint4*>(r + rb0 + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
+            if (kc == 0) reinterpret_cast<float*>(r)[m] = sx;
+        }
+    };
+    // The CTA's sum of the threads' (hi, lo): a fixed tree over the lanes, then the
+    // warps in order (thread 0); every thread returns with __syncthreads behind it.
+    auto cta_sum = [&](float hi, float lo) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o), ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+            ff_add(hi, lo, oh, ol);
+        }
+        if ((threadIdx.x & 31) == 0) {
+            part_hi[threadIdx.x >> 5] = hi;
+            part_lo[threadIdx.x >> 5] = lo;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float th = part_hi[0], tl = part_lo[0];
+            for (int w = 1; w < kThreads / 32; ++w) ff_add(th, tl, part_hi[w], part_lo[w]);
+            slice_sum[0] = th;
+            slice_sum[1] = tl;
+        }
+        __syncthreads();
+    };
+
+    if (one_cta_rows(kind, K)) {
+        // RMSNORM of at most kRowMax inputs: every CTA of the row sums the whole row
+        // itself (thread t: blocks t, t + 256, t + 512 in increasing k, all in
+        // registers), so no CTA waits for another; it then writes the outputs of its
+        // slice's blocks among them.
+        const int64_t nb = K / 8;
+        float a[kRowKeep][8], zero[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zero[e] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kRowKeep; ++j) {
+            const int64_t b = threadIdx.x + (int64_t)j * kThreads;
+            if (b < nb) inputs8(yr, K, 8 * b, kind, vec, a[j], zero);
+        }
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kRowKeep; ++j) {
+            if ((int64_t)threadIdx.x + (int64_t)j * kThreads < nb) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float v = a[j][e];
+                    const float p = __fmul_rn(v, v);
+                    ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
+                }
+            }
+        }
+        cta_sum(hi, lo);
+        const fpair inv = row_scale(slice_sum[0], slice_sum[1], K, eps_hi, eps_lo);
+#pragma unroll
+        for (int j = 0; j < kRowKeep; ++j) {
+            const int64_t b = threadIdx.x + (int64_t)j * kThreads;
+            emit(8 * b, b < nb && 8 * b >= k0 && 8 * b < k1, a[j], zero, inv.hi, inv.lo);
+        }
+        return;
+    }
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8; // 8-input blocks of this slice; thread t takes t, t + 256, ...
+
+    // 1. the slice's sum of squares: each thread's blocks in increasing k; the first kKeep
+    //    blocks stay in registers for step 2 (all their loads in flight together)
     float keep_a[kKeep][8], keep_b[kKeep][8];
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
@@ -216,90 +344,46 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
             ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
         }
     }
-    // fixed tree: lanes, then warps in order
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o), ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
-        ff_add(hi, lo, oh, ol);
-    }
-    if ((threadIdx.x & 31) == 0) {
-        part_hi[threadIdx.x >> 5] = hi;
-        part_lo[threadIdx.x >> 5] = lo;
+    cta_sum(hi, lo);
+    cluster.sync();                                   // every slice's sum is in its CTA's shared memory
+    if (threadIdx.x < 32) {
+        // the slices' sums fetched together (lane r: slice r), then added in rank order
+        const int r = (int)threadIdx.x;
+        float oh = 0.0f, ol = 0.0f;
+        if (r < S) {
+            const float* other = cluster.map_shared_rank(slice_sum, r);
+            oh = other[0];
+            ol = other[1];
+        }
+        float th = 0.0f, tl = 0.0f;
+        for (int j = 0; j < S; ++j)
+            ff_add(th, tl, __shfl_sync(0xFFFFFFFFu, oh, j), __shfl_sync(0xFFFFFFFFu, ol, j));
+        if (r == 0) {
+            const fpair inv = row_scale(th, tl, K, eps_hi, eps_lo);
+            inv_s[0] = inv.hi;
+            inv_s[1] = inv.lo;
+        }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float th = part_hi[0], tl = part_lo[0];
-        for (int w = 1; w < kThreads / 32; ++w) ff_add(th, tl, part_hi[w], part_lo[w]);
-        slice_sum[0] = th;
-        slice_sum[1] = tl;
-    }
-    cluster.sync();                                   // every slice's sum is in its CTA's shared memory
-    if (threadIdx.x == 0) {
-        float th = 0.0f, tl = 0.0f;
-        for (int r = 0; r < S; ++r) {                 // slices in rank order
-            const float* other = cluster.map_shared_rank(slice_sum, r);
-            ff_add(th, tl, other[0], other[1]);
-        }
-        inv_s = 1.0 / sqrt(((double)th + (double)tl) / (double)K + eps);
-    }
-    cluster.sync();                                   // no CTA leaves while another still reads its sum
-    const double inv = inv_s;
-    const float inv_f = (float)inv;
-    const float inv_lo = (float)(inv - (double)inv_f);
+    // the other CTAs may leave once every thread has arrived (this CTA's sum has been
+    // read by then); the wait is at the end, after the outputs
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    const float inv_f = inv_s[0];
+    const float inv_lo = inv_s[1];
 
-    // 2. the outputs, block by block (uniform over the CTA: whole warps take part)
-    const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
-    auto emit = [&](int64_t b0, const float (&a)[8], const float (&bv)[8]) {
-        const int64_t b = b0 + threadIdx.x;
-        const bool active = b < nblk;
-        const int64_t kb = k0 + 8 * b;                // first input of the block
-        uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        if (active) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                h[e] = output_bits(value_f(a[e], bv[e], kind), a[e], bv[e], kind, inv_f, inv_lo);
-        }
-        if (rec == nullptr) {
-            if (active) {
-                uint4 o;
-                o.x = h[0] | (h[1] << 16);
-                o.y = h[2] | (h[3] << 16);
-                o.z = h[4] | (h[5] << 16);
-                o.w = h[6] | (h[7] << 16);
-                *reinterpret_cast<uint4*>(x + (int64_t)m * K + kb) = o;
-            }
-            return;
-        }
-        // record mode: the group sum X, the 8 values in increasing k, then the 8 blocks of the
-        // group (8 consecutive lanes: slices are whole groups) by a fixed xor tree
-        float sx = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sx = __fadd_rn(sx, __uint_as_float(h[e] << 16));
-        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 1));
-        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 2));
-        sx = __fadd_rn(sx, __shfl_xor_sync(0xFFFFFFFFu, sx, 4));
-        if (active) {
-            const int64_t g = kb / 64;
-            const int kc = (int)((kb / 8) & 7);
-            uint8_t* r = rec + g * rb;
-            uint4 o;                                  // pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), scaled
-            o.x = q4::tm::bf16x2_mul(h[0] | (h[4] << 16), q4::tm::kXScaleEven);
-            o.y = q4::tm::bf16x2_mul(h[1] | (h[5] << 16), q4::tm::kXScaleOdd);
-            o.z = q4::tm::bf16x2_mul(h[2] | (h[6] << 16), q4::tm::kXScaleEven);
-            o.w = q4::tm::bf16x2_mul(h[3] | (h[7] << 16), q4::tm::kXScaleOdd);
-            *reinterpret_cast<uint4*>(r + rb0 + (m >> 3) * 1024 + kc * 128 + (m & 7) * 16) = o;
-            if (kc == 0) reinterpret_cast<float*>(r)[m] = sx;
-        }
-    };
+    // 2. the outputs, block by block
 #pragma unroll
     for (int u = 0; u < kKeep; ++u)
-        if ((int64_t)u * kThreads < nblk) emit((int64_t)u * kThreads, keep_a[u], keep_b[u]);
+        if ((int64_t)u * kThreads < nblk)
+            emit(k0 + 8 * ((int64_t)u * kThreads + threadIdx.x), (int64_t)u * kThreads + threadIdx.x < nblk, keep_a[u],
+                 keep_b[u], inv_f, inv_lo);
     for (int64_t b0 = (int64_t)kKeep * kThreads; b0 < nblk; b0 += kThreads) {
         float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         float bv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         if (b0 + threadIdx.x < nblk) inputs8(yr, K, k0 + 8 * (b0 + threadIdx.x), kind, vec, a, bv);
-        emit(b0, a, bv);
+        emit(k0 + 8 * (b0 + threadIdx.x), b0 + threadIdx.x < nblk, a, bv, inv_f, inv_lo);
     }
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");   // no CTA leaves while another reads its sum
 }
 
 }  // namespace glue

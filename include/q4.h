@@ -137,8 +137,9 @@ q4_status q4_matmul_noalloc(const void* x, const void* W, int M, int64_t N, int6
  *   SWIGLU_RMSNORM: v_k = silu(y[m, k]) * y[m, K_next + k]       (N_prev == 2 K_next)
  *   x[m, k] = bf16_RNE( v_k / sqrt( mean_k v_k^2 + 1e-6 ) ),  silu(a) = a / (1 + e^-a)
  * Accuracy: the sum of squares is carried in about 48 bits and the scale formed
- * in double.  RMSNORM: the one rounding to bf16 matches an all-double
- * evaluation except where the value lies within about 1e-14 of a bf16 midpoint.
+ * as a float pair (relative error below 3e-14).  RMSNORM: the one rounding to
+ * bf16 matches an all-double evaluation except where the value lies within
+ * about 1e-13 of a bf16 midpoint.
  * SWIGLU: silu(a) * b is formed in fp32 (within 9 float ulps), and recomputed in
  * float pairs (about 1e-14) near a bf16 midpoint; the scale agrees with an
  * all-double one to about 1e-8 (at worst 5e-7), so an output may differ by one

@@ -100,7 +100,9 @@ def _run_by_layers(layers, x0, checks=True, sample=None, tag=""):
     return y
 
 
+# RMSNORM up to 6144 inputs: every CTA sums its row alone; beyond, and SWIGLU: a cluster per row
 @pytest.mark.parametrize("kind,N_prev,K", [(q4.GLUE_RMSNORM, 640, 576), (q4.GLUE_RMSNORM, 5120, 5120),
+                                           (q4.GLUE_RMSNORM, 16640, 6144), (q4.GLUE_RMSNORM, 10240, 8192),
                                            (q4.GLUE_SWIGLU_RMSNORM, 2 * 17408, 17408),
                                            (q4.GLUE_SWIGLU_RMSNORM, 2048, 1024)])
 def test_glue_against_oracle(kind, N_prev, K):
