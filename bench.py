@@ -928,8 +928,9 @@ def run_full_pass(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
                      "algorithmic_bytes_per_launch": step_bytes // n_mm,
                      "note": "whole step (matmul and glue launches) timed; a lower bound for the matmul kernel"},
-        # matmul per layer, glue between (writing the next layer's x records), x records for layer 0
-        "gpu_launches": (n_mm + (n_mm - 1) + 1) * args.steps,
+        # one matmul per layer (the first builds its own x records) and one glue between
+        # consecutive layers (writing the next layer's x records)
+        "gpu_launches": (n_mm + (n_mm - 1)) * args.steps,
         "clocks": clocks, "e2e": e2e,
     }
     if not args.no_cpu_baseline:
