@@ -13,7 +13,7 @@
 // of a contiguous slice of the row made of whole groups of 64 inputs, so a
 // step's glue runs on up to 8*M SMs instead of M.  S and the slices depend on K
 // only.  RMSNORM rows of at most 6144 inputs: every CTA forms the whole row's
-// sum of squares itself (thread t: 8-input blocks t, t + 256, t + 512), so no
+// sum of squares itself (thread t: 8-input blocks t, t + 288, t + 576), so no
 // CTA waits for another.  Otherwise the S CTAs of a row form a cluster and
 // each sums its own slice (the order below).
 //
@@ -27,13 +27,13 @@
 // single-precision pipes.  The sum of squares is kept as an unevaluated pair of
 // floats (each square split exactly by an fma, the pairs added with error-free
 // two-sums), which carries about 48 significant bits.  Each thread takes 8-input
-// blocks (t, t + 256, ... of the row, or of its slice in a cluster) and adds their
+// blocks (t, t + 288, ... of the row, or of its slice in a cluster) and adds their
 // squares in increasing k; the threads' sums go through a fixed tree over lanes
 // and warps; in a cluster the slices are combined in rank order through
 // distributed shared memory (their sums fetched together).  The scale
 // 1/sqrt(ss/K + eps) is formed as a float pair (one Newton step from the float
 // value; relative error below 3e-14).  y is read once per CTA: a thread's first
-// blocks stay in registers for the outputs (all of a slice up to 4096 inputs,
+// blocks stay in registers for the outputs (all of a slice up to 4608 inputs,
 // or of a row up to 6144).
 //   RMSNORM: v is an exact float, so v * scale is formed as a normalised float
 //   pair and rounded to bf16 from it (the dropped 16 bits of the high part, and
@@ -66,18 +66,19 @@ namespace glue {
 
 using namespace q4::pair;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;                 // 9 warps: a SWIGLU slice of 2176 inputs is one 8-input block per thread
 constexpr int kMaxSlices = 8;                 // portable cluster size
 constexpr int64_t kSliceMin = 1024;           // inputs per slice below which fewer slices are used
 // An output computed in float is trusted unless its low 16 bits (the bits
 // bf16 rounding drops) are within this many float ulps of the halfway point.
 constexpr int kTieMarginSwiglu = 10;          // SWIGLU: the fp32 output is within 9 float ulps of exact
-constexpr int kKeep = 2;                      // 8-input blocks per thread held in registers (slices <= 4096 inputs)
+constexpr int kKeep = 2;                      // 8-input blocks per thread held in registers (slices <= 4608 inputs)
 
 // RMSNORM rows of at most kRowMax inputs: every CTA of the row forms the row's sum
 // of squares itself, kRowKeep 8-input blocks per thread (no cluster).
 constexpr int kRowKeep = 3;
-constexpr int64_t kRowMax = (int64_t)kRowKeep * kThreads * 8;   // 6144
+constexpr int64_t kRowMax = 6144;
+static_assert(kRowMax <= (int64_t)kRowKeep * kThreads * 8, "a row of kRowMax inputs fits the threads' registers");
 
 __host__ __device__ inline bool one_cta_rows(int kind, int64_t K) { return kind == 1 && K <= kRowMax; }
 
@@ -214,12 +215,14 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     // The block of inputs kb .. kb+7 (of this CTA's slice when active): its 8 outputs
     // to x, or into the next matmul's records (uniform over the CTA: whole warps call it).
     const int rb = q4::tm::rec_bytes(rec_w), rb0 = q4::tm::rec_b(rec_w);
-    auto emit = [&](int64_t kb, bool active, const float (&a)[8], const float (&bv)[8], float inv_f, float inv_lo) {
+    // v: the 8 values (value_f of a and bv).
+    auto emit = [&](int64_t kb, bool active, const float (&v)[8], const float (&a)[8], const float (&bv)[8],
+                    float inv_f, float inv_lo) {
         uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (active) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                h[e] = output_bits(value_f(a[e], bv[e], kind), a[e], bv[e], kind, inv_f, inv_lo);
+                h[e] = output_bits(v[e], a[e], bv[e], kind, inv_f, inv_lo);
         }
         if (rec == nullptr) {
             if (active) {
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
 
     if (one_cta_rows(kind, K)) {
         // RMSNORM of at most kRowMax inputs: every CTA of the row sums the whole row
-        // itself (thread t: blocks t, t + 256, t + 512 in increasing k, all in
+        // itself (thread t: blocks t, t + 288, t + 576 in increasing k, all in
         // registers), so no CTA waits for another; it then writes the outputs of its
         // slice's blocks among them.
         const int64_t nb = K / 8;
@@ -306,17 +309,17 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
 #pragma unroll
         for (int j = 0; j < kRowKeep; ++j) {
             const int64_t b = threadIdx.x + (int64_t)j * kThreads;
-            emit(8 * b, b < nb && 8 * b >= k0 && 8 * b < k1, a[j], zero, inv.hi, inv.lo);
+            emit(8 * b, b < nb && 8 * b >= k0 && 8 * b < k1, a[j], a[j], zero, inv.hi, inv.lo);
         }
         return;
     }
 
     cg::cluster_group cluster = cg::this_cluster();
-    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8; // 8-input blocks of this slice; thread t takes t, t + 256, ...
+    const int64_t nblk = (k1 > k0 ? k1 - k0 : 0) / 8; // 8-input blocks of this slice; thread t takes t, t + 288, ...
 
     // 1. the slice's sum of squares: each thread's blocks in increasing k; the first kKeep
     //    blocks stay in registers for step 2 (all their loads in flight together)
-    float keep_a[kKeep][8], keep_b[kKeep][8];
+    float keep_a[kKeep][8], keep_b[kKeep][8], keep_v[kKeep][8];
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
     for (int u = 0; u < kKeep; ++u) {
@@ -329,6 +332,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float v = value_f(keep_a[u][e], keep_b[u][e], kind);
+                keep_v[u][e] = v;                     // for the outputs
                 const float p = __fmul_rn(v, v);
                 ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
             }
@@ -375,13 +379,16 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
 #pragma unroll
     for (int u = 0; u < kKeep; ++u)
         if ((int64_t)u * kThreads < nblk)
-            emit(k0 + 8 * ((int64_t)u * kThreads + threadIdx.x), (int64_t)u * kThreads + threadIdx.x < nblk, keep_a[u],
-                 keep_b[u], inv_f, inv_lo);
+            emit(k0 + 8 * ((int64_t)u * kThreads + threadIdx.x), (int64_t)u * kThreads + threadIdx.x < nblk, keep_v[u],
+                 keep_a[u], keep_b[u], inv_f, inv_lo);
     for (int64_t b0 = (int64_t)kKeep * kThreads; b0 < nblk; b0 += kThreads) {
         float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         float bv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         if (b0 + threadIdx.x < nblk) inputs8(yr, K, k0 + 8 * (b0 + threadIdx.x), kind, vec, a, bv);
-        emit(k0 + 8 * (b0 + threadIdx.x), b0 + threadIdx.x < nblk, a, bv, inv_f, inv_lo);
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = value_f(a[e], bv[e], kind);
+        emit(k0 + 8 * (b0 + threadIdx.x), b0 + threadIdx.x < nblk, v, a, bv, inv_f, inv_lo);
     }
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");   // no CTA leaves while another reads its sum
 }
