@@ -20,8 +20,9 @@
 // Two outputs.  x mode writes x_next as bf16 [M, K].  Record mode (inside a
 // chained pass, when the next matmul runs the tensor-memory kernel) writes the
 // next matmul's x records instead -- the same bf16 values, permuted and scaled
-// into the record layout, and the group sums X added in the record kernel's
-// order -- so that matmul needs no record kernel and x_next is never stored.
+// into the record layout, and the group sums X added in the order of the
+// matmul's own record build -- so that matmul builds none and x_next is never
+// stored.
 //
 // Arithmetic: the definition is evaluated as if in double, on the
 // single-precision pipes.  The sum of squares is kept as an unevaluated pair of
