@@ -579,7 +579,7 @@ __device__ __noinline__ void finish_tile(const float* __restrict__ partials, flo
 #pragma unroll
     for (int m = 0; m < MT; ++m) v[m] = 0.0f;
     // ranges in increasing order, kB at a time with their loads in flight together
-    constexpr int kB = MT <= 8 ? 4 : (MT <= 16 ? 2 : 1);
+    constexpr int kB = MT <= 8 ? 4 : 2;
     for (int rb = r_first; rb <= r_last; rb += kB) {
         float pv[kB][MT];
 #pragma unroll
