@@ -451,7 +451,10 @@ q4_status check_glue_args(const float* y, int M, int64_t n_prev, int64_t K, int 
 // matmul's x records (row width rec_w) to rec instead.
 q4_status launch_glue(const float* y, int M, int64_t n_prev, int64_t K, int kind, void* x, cudaStream_t stream,
                       uint8_t* rec = nullptr, int rec_w = 16) {
-    const int S = q4::glue::slices(K);
+    // rows every CTA sums alone: 8 CTAs (one per 640 inputs at K = 5120) spread the outputs widest
+    // (measured: 1, 2, 5 and 16 per row were slower); otherwise slices(K), as a cluster
+    const int S = q4::glue::one_cta_rows(kind, K) ? (int)std::min<int64_t>(q4::glue::kMaxSlices, K / 64)
+                                                  : q4::glue::slices(K);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S, (unsigned)M);
     cfg.blockDim = dim3(q4::glue::kThreads);

@@ -9,13 +9,14 @@
 // norms) are not on the matmul path; this fixed, bounded stand-in keeps the
 // values of a long chain of linears in range.
 //
-// Work split: S = slices(K) CTAs per row (at most 8), each writing the outputs
-// of a contiguous slice of the row made of whole groups of 64 inputs, so a
-// step's glue runs on up to 8*M SMs instead of M.  S and the slices depend on K
-// only.  RMSNORM rows of at most 6144 inputs: every CTA forms the whole row's
-// sum of squares itself (thread t: 8-input blocks t, t + 288, t + 576), so no
-// CTA waits for another.  Otherwise the S CTAs of a row form a cluster and
-// each sums its own slice (the order below).
+// Work split: S CTAs per row (at most 8), each writing the outputs of a
+// contiguous slice of the row made of whole groups of 64 inputs, so a step's
+// glue runs on up to 8*M SMs instead of M.  S and the slices depend on K and
+// the kind only.  RMSNORM rows of at most 6144 inputs: S = 8 (fewer if K has
+// fewer groups), and every CTA forms the whole row's sum of squares itself
+// (thread t: 8-input blocks t, t + 288, t + 576), so no CTA waits for another.
+// Otherwise S = slices(K), the S CTAs of a row form a cluster and each sums its
+// own slice (the order below).
 //
 // Two outputs.  x mode writes x_next as bf16 [M, K].  Record mode (inside a
 // chained pass, when the next matmul runs the tensor-memory kernel) writes the
