@@ -56,6 +56,8 @@ def parse_args():
                    "the LM head and the full pass)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=64, help="full_pass only: the first LAYERS of the 64 layers "
+                   "(4 linears each, no LM head; a small case for profiler captures)")
     return p.parse_args()
 
 
@@ -823,6 +825,14 @@ def run_full_pass(args, rank, world, local_rank):
     M = 16
     spec = si.full_pass_spec()
     _, desc = workload_spec("full_pass")
+    if not 1 <= args.layers <= 64:
+        raise SystemExit("--layers must be in 1..64")
+    if args.layers < 64:
+        # a small case of the same kernels: the first layers only, the last linear ending the step
+        spec = spec[:4 * args.layers]
+        spec[-1] = (spec[-1][0], spec[-1][1], 0)
+        desc = (f"the first {args.layers} of the 64 layers of the 27B-shaped verify pass (4 linears each, no LM "
+                f"head; a profiling case, not the full pass), M=16, chained through q4_decode_step")
     weight_bytes = sum(N * K * 9 // 16 for N, K, _ in spec)
     n_mm = len(spec)
     # algorithmic bytes of the step: every weight once, each layer's x and y once

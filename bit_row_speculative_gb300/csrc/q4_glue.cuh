@@ -371,9 +371,10 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         }
     }
     __syncthreads();
-    // the other CTAs may leave once every thread has arrived (this CTA's sum has been
-    // read by then); the wait is at the end, after the outputs
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    // the other CTAs may leave once every thread has arrived: the only accesses it
+    // orders are warp 0's reads of their sums, whose values are already in use, so the
+    // arrival needs no release; the wait is at the end, after the outputs
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const float inv_f = inv_s[0];
     const float inv_lo = inv_s[1];
 
