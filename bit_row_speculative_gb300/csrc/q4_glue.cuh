@@ -31,8 +31,9 @@
 // two-sums), which carries about 48 significant bits.  Each thread takes 8-input
 // blocks (t, t + 288, ... of the row, or of its slice in a cluster) and adds their
 // squares in increasing k; the threads' sums go through a fixed tree over lanes
-// and warps; in a cluster the slices are combined in rank order through
-// distributed shared memory (their sums fetched together).  The scale
+// and warps; in a cluster each CTA pushes its slice's sum into every CTA's
+// shared memory (distributed shared memory) before one cluster barrier, and
+// every CTA adds the slices' sums in rank order.  The scale
 // 1/sqrt(ss/K + eps) is formed as a float pair (one Newton step from the float
 // value; relative error below 3e-14).  y is read once per CTA: a thread's first
 // blocks stay in registers for the outputs (all of a slice up to 4608 inputs,
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
     namespace cg = cooperative_groups;
     __shared__ float part_hi[kThreads / 32], part_lo[kThreads / 32];
     __shared__ float slice_sum[2];
+    __shared__ float2 sums[kMaxSlices];             // cluster rows: every slice's sum, in rank order
     __shared__ float inv_s[2];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");     // y comes from the preceding kernel
@@ -350,20 +352,32 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
             ff_add(hi, lo, p, __fmaf_rn(v, v, -p));
         }
     }
-    cta_sum(hi, lo);
-    cluster.sync();                                   // every slice's sum is in its CTA's shared memory
+    // the slice's sum (the same tree as cta_sum), pushed by thread 0 into slot s of
+    // every CTA's sums, so that after the cluster barrier each CTA reads its own
+    // shared memory only (and may leave without waiting for the others)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o), ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+        ff_add(hi, lo, oh, ol);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        part_hi[threadIdx.x >> 5] = hi;
+        part_lo[threadIdx.x >> 5] = lo;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float th = part_hi[0], tl = part_lo[0];
+        for (int w = 1; w < kThreads / 32; ++w) ff_add(th, tl, part_hi[w], part_lo[w]);
+        for (int r = 0; r < S; ++r) cluster.map_shared_rank(sums, r)[s] = make_float2(th, tl);
+    }
+    cluster.sync();                                   // every CTA's sums hold every slice's sum
     if (threadIdx.x < 32) {
-        // the slices' sums fetched together (lane r: slice r), then added in rank order
+        // the slices' sums (lane r: slice r), added in rank order
         const int r = (int)threadIdx.x;
-        float oh = 0.0f, ol = 0.0f;
-        if (r < S) {
-            const float* other = cluster.map_shared_rank(slice_sum, r);
-            oh = other[0];
-            ol = other[1];
-        }
+        const float2 o = r < S ? sums[r] : make_float2(0.0f, 0.0f);
         float th = 0.0f, tl = 0.0f;
         for (int j = 0; j < S; ++j)
-            ff_add(th, tl, __shfl_sync(0xFFFFFFFFu, oh, j), __shfl_sync(0xFFFFFFFFu, ol, j));
+            ff_add(th, tl, __shfl_sync(0xFFFFFFFFu, o.x, j), __shfl_sync(0xFFFFFFFFu, o.y, j));
         if (r == 0) {
             const fpair inv = row_scale(th, tl, K, eps_hi, eps_lo);
             inv_s[0] = inv.hi;
@@ -371,10 +385,6 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         }
     }
     __syncthreads();
-    // the other CTAs may leave once every thread has arrived: the only accesses it
-    // orders are warp 0's reads of their sums, whose values are already in use, so the
-    // arrival needs no release; the wait is at the end, after the outputs
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const float inv_f = inv_s[0];
     const float inv_lo = inv_s[1];
 
@@ -393,7 +403,6 @@ __global__ void __launch_bounds__(kThreads) glue_kernel(const float* __restrict_
         for (int e = 0; e < 8; ++e) v[e] = value_f(a[e], bv[e], kind);
         emit(k0 + 8 * (b0 + threadIdx.x), b0 + threadIdx.x < nblk, v, a, bv, inv_f, inv_lo);
     }
-    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");   // no CTA leaves while another reads its sum
 }
 
 }  // namespace glue
