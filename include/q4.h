@@ -199,7 +199,10 @@ q4_status q4_decode_step(const q4_layer* layers, int n_layers, const void* x0, i
  *           unique); -1 past top_k.
  *   probs : device, fp32 [M, 32]: p_j = exp((l_j - l_0)/T) / sum over the
  *           top_k; the shortest prefix whose cumulative probability reaches
- *           top_p is kept and renormalized; 0 for the rest.  Computed in double.
+ *           top_p is kept and renormalized; 0 for the rest.  Computed in
+ *           float pairs (about 48 significant bits, so they round as
+ *           double-precision values would; an exponential below e^-60 in
+ *           double).
  * All pointers 16-byte aligned.  Asynchronous on `stream`; uses the library's
  * per-device scratch (the same ordering rules as q4_matmul). */
 q4_status q4_topk_probs(const float* logits, int M, int64_t N, int top_k, float temperature, float top_p,
